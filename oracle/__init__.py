@@ -1,0 +1,174 @@
+"""fp64 CPU oracle for mean-query column-sparse attention (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by the package's smoke
+check and by the benchmark's CPU-baseline leg, never by the product path.
+The arithmetic lives in ``oracle.c``; this file only marshals numpy arrays.
+It shares no code with the CUDA path.
+
+Modes follow the C side: 0 = TOPK, 1 = THRESHOLD, 2 = MASS.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+TOPK, THRESHOLD, MASS = 0, 1, 2
+MODES = {"topk": TOPK, "threshold": THRESHOLD, "mass": MASS}
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` with gcc (IEEE fp64, no FMA
+    contraction, so x86 and Arm hosts produce the same bits)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-Wall", "-ffp-contract=off", "-fPIC",
+                        "-shared", "-pthread", "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _configure(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    i64, p = ctypes.c_int64, ctypes.c_void_p
+    lib.oracle_mean_query.argtypes = [p, i64, i64, i64, i64, i64, p, i64, p]
+    lib.oracle_group_scores.argtypes = [p, p, i64, i64, i64, i64, i64, i64,
+                                        ctypes.c_double, p, i64, p, ctypes.c_int]
+    lib.oracle_select.argtypes = [p, i64, i64, ctypes.c_int, i64, ctypes.c_double,
+                                  ctypes.c_double, p, p, p, ctypes.c_int]
+    lib.oracle_forward.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64,
+                                   ctypes.c_double, p, p, p, i64, p, p, ctypes.c_int]
+    for f in (lib.oracle_mean_query, lib.oracle_group_scores, lib.oracle_select,
+              lib.oracle_forward):
+        f.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _configure(ctypes.CDLL(build()))
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _bits(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("oracle inputs are bf16 bit patterns (uint16)")
+    return a
+
+
+def _units(units, total):
+    if units is None:
+        units = np.arange(total, dtype=np.int64)
+    return np.ascontiguousarray(units, dtype=np.int64)
+
+
+def mean_query(q, M: int, units=None) -> np.ndarray:
+    """q: uint16 [B,H,Nq,d] -> float64 [n_units, d]."""
+    q = _bits(q)
+    B, H, Nq, d = q.shape
+    G = -(-Nq // M)
+    units = _units(units, B * H * G)
+    out = np.empty((units.size, d), dtype=np.float64)
+    rc = _load().oracle_mean_query(_ptr(q), B, H, Nq, d, M, _ptr(units), units.size, _ptr(out))
+    if rc:
+        raise ValueError("oracle_mean_query rejected its arguments")
+    return out
+
+
+def group_scores(q, k, M: int, scale: float, units=None, threads: int | None = None):
+    """Mean-query scores: float64 [n_units, Nk]."""
+    q, k = _bits(q), _bits(k)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    G = -(-Nq // M)
+    units = _units(units, B * H * G)
+    out = np.empty((units.size, Nk), dtype=np.float64)
+    rc = _load().oracle_group_scores(_ptr(q), _ptr(k), B, H, Nq, Nk, d, M, float(scale),
+                                     _ptr(units), units.size, _ptr(out),
+                                     threads or default_threads())
+    if rc:
+        raise ValueError("oracle_group_scores rejected its arguments")
+    return out
+
+
+def select(scores, mode, topk: int = 0, tau: float = 0.0, rho: float = 0.99,
+           threads: int | None = None):
+    """Returns (lists, cut): ascending int32 index arrays per row, cut scores."""
+    scores = np.ascontiguousarray(scores, dtype=np.float64)
+    n_rows, Nk = scores.shape
+    mode = MODES.get(mode, mode)
+    counts = np.empty(n_rows, dtype=np.int64)
+    idx = np.empty((n_rows, max(Nk, 1)), dtype=np.int32)
+    cut = np.empty(n_rows, dtype=np.float64)
+    rc = _load().oracle_select(_ptr(scores), n_rows, Nk, int(mode), int(topk), float(tau),
+                               float(rho), _ptr(counts), _ptr(idx), _ptr(cut),
+                               threads or default_threads())
+    if rc:
+        raise ValueError("oracle_select rejected its arguments")
+    return [idx[r, :counts[r]].copy() for r in range(n_rows)], cut
+
+
+def build_index(q, k, M: int, scale: float, mode, topk: int = 0, tau: float = 0.0,
+                rho: float = 0.99, units=None, threads: int | None = None):
+    """Scores + selection for the listed units: (lists, cut, scores)."""
+    sc = group_scores(q, k, M, scale, units, threads)
+    lists, cut = select(sc, mode, topk, tau, rho, threads)
+    return lists, cut, sc
+
+
+def to_csr(lists):
+    """Concatenate per-row lists into (row_ptr int64, col_idx int32)."""
+    counts = np.array([len(x) for x in lists], dtype=np.int64)
+    row_ptr = np.zeros(len(lists) + 1, dtype=np.int64)
+    np.cumsum(counts, out=row_ptr[1:])
+    col = np.concatenate(lists).astype(np.int32) if lists else np.zeros(0, np.int32)
+    return row_ptr, col
+
+
+def forward(q, k, v, M: int, scale: float, row_ptr, col_idx, units=None,
+            threads: int | None = None):
+    """Restricted attention of the listed units.
+
+    row_ptr has B*H*G+1 entries indexed by unit id.  Returns o float64
+    [n_units, M, d] (rows past Nq are zero) and lse float64 [n_units, M].
+    """
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    G = -(-Nq // M)
+    units = _units(units, B * H * G)
+    row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int64)
+    col_idx = np.ascontiguousarray(col_idx, dtype=np.int32)
+    if row_ptr.size != B * H * G + 1:
+        raise ValueError("row_ptr must have B*H*G+1 entries")
+    if col_idx.size == 0:
+        col_idx = np.zeros(1, dtype=np.int32)
+    o = np.empty((units.size, M, d), dtype=np.float64)
+    lse = np.empty((units.size, M), dtype=np.float64)
+    rc = _load().oracle_forward(_ptr(q), _ptr(k), _ptr(v), B, H, Nq, Nk, d, M, float(scale),
+                                _ptr(row_ptr), _ptr(col_idx), _ptr(units), units.size,
+                                _ptr(o), _ptr(lse), threads or default_threads())
+    if rc:
+        raise ValueError("oracle_forward rejected its arguments")
+    return o, lse
