@@ -33,7 +33,8 @@
  *  - THRESHOLD keeps j with p_j = exp(sigma_j - LSE_all) >= tau, where
  *    LSE_all is over all Nk keys; if none qualifies the top-ranked key is kept.
  *  - MASS keeps the shortest ranked prefix whose sum of p_j reaches rho
- *    (all keys if the total falls short through rounding).
+ *    (all keys if the total falls short through rounding, and all keys for
+ *    rho >= 1, since every p_j is positive).
  *  - the reported cut is the score of the last key taken (TOPK, MASS) or
  *    ln(tau) + LSE_all (THRESHOLD).
  *
@@ -238,8 +239,10 @@ static void select_row(void* vctx, int64_t r) {
       if (n < 1) n = 1;
       cut = log(c->tau) + lse;
     } else {
-      /* shortest ranked prefix with sum p >= rho */
+      /* shortest ranked prefix with sum p >= rho; rho >= 1 needs every key,
+       * since each p_j is positive */
       double acc = 0.0;
+      if (c->rho >= 1.0) n = Nk;
       while (n < Nk) {
         acc += exp(order[n].score - lse);
         ++n;
