@@ -1,0 +1,388 @@
+"""Benchmark: one step = the whole hot path (sparse_attn_build_index +
+sparse_attn_forward) over one synthetic attention layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is effective TFLOP/s on kept scores
+(4*d flops per kept query-key pair) for build + forward, inputs resident in
+HBM; `e2e` is the same metric with host buffers (H2D of q, k, v and D2H of
+o, lse inside the timed region); `roofline` is the forward kernel against
+the measured bf16 tensor peak.  `--impl reference` times the fp64 CPU
+oracle on a bounded sample of the same workload.
+Under torchrun (N > 1) every rank runs the full layer on its own GPU (weak
+scaling; heads are independent, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "effective TFLOP/s on kept scores (4·d/pair) & ms/layer; % of GB300 dense BF16 TC peak"
+DEFAULT_WORKLOAD = "wan16k_top20"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+KERNELS_PER_STEP = 6  # meanq, score, select, scan, emit, forward
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "video_dit_sparse_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel, {}).get(workload)
+    if not rec or rec.get("source_hash") != source_hash(*rec.get("sources", [])):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def kept_pairs(row_ptr: np.ndarray, B, H, Nq, M) -> int:
+    """sum over units of |group rows| * |kept keys|."""
+    G = -(-Nq // M)
+    counts = np.diff(row_ptr).reshape(B * H, G)
+    rows = np.full(G, M, dtype=np.int64)
+    rows[-1] = Nq - (G - 1) * M
+    return int((counts * rows[None, :]).sum())
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_ms: float, local_units: float, world: int, group=None):
+    """Max step time over ranks and total units (all-reduce on the host
+    backend; the only collective in the benchmark)."""
+    if world == 1:
+        return local_ms, local_units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample(w, x, budget_s: float, threads: int):
+    """Times the fp64 oracle (mean-query scores + selection + restricted
+    attention) on a growing sample of units until about `budget_s` seconds of
+    work; returns (effective TFLOP/s, description, threads)."""
+    import oracle
+    rows = w.B * w.H * w.G
+    rng = np.random.default_rng(7)
+    order = rng.permutation(rows)
+    n = min(threads, rows)
+    spent, pairs, done = 0.0, 0, 0
+    while True:
+        units = np.sort(order[done:done + n]).astype(np.int64)
+        t0 = time.perf_counter()
+        lists, _, _ = oracle.build_index(x["q"], x["k"], w.group, w.scale, w.mode, topk=w.topk,
+                                         tau=w.threshold, rho=w.mass, units=units, threads=threads)
+        counts = np.zeros(rows, dtype=np.int64)
+        counts[units] = [len(l) for l in lists]
+        row_ptr = np.zeros(rows + 1, dtype=np.int64)
+        np.cumsum(counts, out=row_ptr[1:])
+        col = np.zeros(row_ptr[-1], dtype=np.int32)
+        for u, l in zip(units, lists):
+            col[row_ptr[u]:row_ptr[u + 1]] = l
+        oracle.forward(x["q"], x["k"], x["v"], w.group, w.scale, row_ptr, col, units, threads)
+        spent += time.perf_counter() - t0
+        for u, l in zip(units, lists):
+            g = u % w.G
+            pairs += (min((g + 1) * w.group, w.Nq) - g * w.group) * len(l)
+        done += units.size
+        if spent >= budget_s or done >= rows:
+            break
+        n = min(rows - done, max(n, int(n * budget_s / max(spent, 1e-3))))
+    tflops = 4.0 * w.d * pairs / spent / 1e12
+    desc = f"{done} of {rows} query groups (seeded), full scoring+selection+attention per group"
+    return tflops, desc, spent
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    from video_dit_sparse_gb300 import inputs as I
+    threads = oracle.default_threads()
+    x = I.make_inputs(w, 0)
+    for _ in range(args.warmup):
+        oracle_sample(w, x, 0.0, threads)
+    times, vals = [], []
+    for _ in range(args.steps):
+        v, desc, spent = oracle_sample(w, x, args.ref_budget, threads)
+        vals.append(v)
+        times.append(spent)
+    value = float(np.mean(vals))
+    ms = 1e3 * float(np.mean(times))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, None),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, pairs):
+    c = {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+         "group": w.group, "selection": {"topk": f"k={w.topk}", "mass": f"rho={w.mass}",
+                                         "threshold": f"tau={w.threshold}"}[w.mode],
+         "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)"}
+    if pairs is not None:
+        c["kept_pairs"] = pairs
+    return c
+
+
+# --------------------------------------------------------------- GPU arm
+def run_ours(args, w):
+    import torch
+    world, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from video_dit_sparse_gb300 import binding as sa
+    from video_dit_sparse_gb300 import inputs as I
+
+    x = I.make_inputs(w, 0)
+    dev = torch.device("cuda", local)
+
+    def host(b):
+        return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    hq, hk, hv = host(x["q"]), host(x["k"]), host(x["v"])
+    q, k, v = hq.to(dev), hk.to(dev), hv.to(dev)
+    stream = torch.cuda.current_stream()
+    p = sa.problem(q, k, w.group, w.scale)
+    ws = torch.empty(sa.sparse_attn_build_index_workspace_size(p), dtype=torch.uint8, device=dev)
+    rows = w.B * w.H * w.G
+    cap = rows * (w.topk if w.mode == "topk" else w.Nk)
+    col = torch.empty(cap, dtype=torch.int32, device=dev)
+    row_ptr = torch.empty(rows + 1, dtype=torch.int64, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sel = sa.sa_select(sa._MODES[w.mode], w.topk, w.threshold, w.mass)
+    nnz_box = sa.ctypes.c_int64(0)
+    sync_nnz = w.mode != "topk"
+
+    def build():
+        st = sa.lib.sparse_attn_build_index(
+            sa.ctypes.byref(p), sa.ctypes.byref(sel), sa._ptr(q), sa._ptr(k), sa._ptr(row_ptr),
+            sa._ptr(col), cap, sa.ctypes.byref(nnz_box) if sync_nnz else None, sa._ptr(ws),
+            ws.numel(), sa._stream(stream))
+        if st:
+            raise sa.SparseAttnError(st, "build_index")
+
+    def fwd(nnz):
+        st = sa.lib.sparse_attn_forward(sa.ctypes.byref(p), sa._ptr(q), sa._ptr(k), sa._ptr(v),
+                                        sa._ptr(row_ptr), sa._ptr(col), nnz, sa._ptr(o),
+                                        sa._ptr(lse), None, sa._stream(stream))
+        if st:
+            raise sa.SparseAttnError(st, "forward")
+
+    def nnz_now():
+        return nnz_box.value if sync_nnz else rows * w.topk
+
+    for _ in range(max(args.warmup, 1)):
+        build()
+        fwd(nnz_now())
+    torch.cuda.synchronize()
+    pairs = kept_pairs(row_ptr.cpu().numpy(), w.B, w.H, w.Nq, w.group)
+    flops = 4.0 * w.d * pairs
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            build()
+            ev[i][1].record(stream)
+            fwd(nnz_now())
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_build = [e[0].elapsed_time(e[1]) for e in ev]
+    t_fwd = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_step = float(np.mean(t_build) + np.mean(t_fwd))
+    ms_max, units_total = aggregate(ms_step, float(flops), world)
+    value = units_total / (ms_max * 1e-3) / 1e12
+
+    # end to end through the C ABI with host buffers
+    e2e_steps = max(3, min(args.steps, 20))
+    h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(e2e_steps):
+        flush.zero_()
+        e0.record(stream)
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        build()
+        fwd(nnz_now())
+        h_o.copy_(o, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_ms_max, _ = aggregate(float(np.mean(e2e_ms)), 0.0, world)
+    e2e_value = units_total / (e2e_ms_max * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+    pk, pk_kind = peaks()
+    fwd_ms = float(np.mean(t_fwd))
+    achieved = flops / (fwd_ms * 1e-3) / 1e12
+    traffic = recorded_traffic("sa_forward_kernel", w.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+                "kernel": "sa_forward_kernel", "peak_source": f"{pk_kind} bf16_tflops (burst)",
+                "frac_of_sustained": achieved / pk.get("bf16_tflops_sustained", pk["bf16_tflops"])}
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(w, pairs),
+            "ms_build_index": float(np.mean(t_build)), "ms_forward": fwd_ms,
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "roofline": roofline,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(3 * q.numel() * 2),
+                    "d2h_bytes_per_step": int(o.numel() * 2 + lse.numel() * 4),
+                    "ms_per_step": e2e_ms_max},
+            "clocks": clocks.summary()}
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.default_threads()
+        cv, desc, spent = oracle_sample(w, x, args.cpu_budget, threads)
+        line["cpu_baseline"] = {"value": cv, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": desc, "seconds": round(spent, 2)}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-budget", type=float, default=4.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from video_dit_sparse_gb300 import inputs as I
+    w = I.preset(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

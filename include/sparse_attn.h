@@ -1,0 +1,188 @@
+/*
+ * sparse_attn.h — C ABI of the column-sparse (Mx1-slice) attention library
+ * (libsparse_attn.so, hand-written CUDA kernels for sm_103a / GB300).
+ *
+ * The operation, as the video-DiT pages state it:
+ *  - FG-Attn review (arXiv 2509.16518), "The pith" and "What carries the
+ *    argument": attention scores are skipped per Mx1 slice — M contiguous
+ *    queries against one key — so each group of M queries keeps its own list
+ *    of key indices, and only those K/V rows are gathered into dense tiles.
+ *  - Chipmunk review (arXiv 2506.03275), "What carries the argument": the
+ *    same idea with [C,1] column chunks, C = 192 voxel-ordered tokens; major
+ *    comment 1 / Alg. 3: the softmax is renormalised over the selected keys
+ *    only (restricted softmax).
+ *  - FG-Attn review, referee comment 2 (§4.4): the list is built without
+ *    training by scoring every key with the group's average query,
+ *    k . q_avg / sqrt(D); LoSA abstract (mlsift.com list): or by keeping the
+ *    smallest key set that retains 99 % of the attention mass.
+ *  - DiT page (woonyee.org), "Self Attention" and "Online Softmax":
+ *    O = softmax(Q K^T / sqrt(d)) V per head, computed tile by tile with a
+ *    running max, running sum and running output.
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are row-major [B, H, N, d] with d contiguous (BHND), bf16.
+ *  - Query group g of a head covers query rows [g*M, min((g+1)*M, Nq));
+ *    G = ceil(Nq / M) groups per head; "rows" of an index are the
+ *    B*H*G (batch, head, group) units in that order.
+ *  - Index lists are CSR: row_ptr int64 [B*H*G + 1], col_idx int32 [nnz];
+ *    the keys of unit u are col_idx[row_ptr[u] .. row_ptr[u+1]).
+ *  - Every pointer argument marked "device" must be a CUDA device (or
+ *    managed) address on the current device; the caller owns all memory.
+ *    q, k, v, o and the workspace must be 16-byte aligned; row_ptr 8-byte;
+ *    col_idx and lse 4-byte.
+ *  - All work is enqueued on `stream` (NULL = legacy default stream) and is
+ *    asynchronous unless a function says it synchronises.  Argument errors
+ *    are returned before anything is enqueued.
+ *  - No function allocates device memory, and none falls back to the CPU.
+ *  - Supported: d in {64, 128}; 1 <= M <= 256; 1 <= Nq, Nk < 2^31.
+ */
+#ifndef SPARSE_ATTN_H
+#define SPARSE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st* sa_stream_t;
+
+typedef enum {
+  SA_OK = 0,
+  SA_ERR_INVALID_ARG = 1,  /* bad pointer, alignment, shape or mode */
+  SA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. d = 96) or no sm_103a device */
+  SA_ERR_CAPACITY = 3,     /* col_capacity smaller than the lists need */
+  SA_ERR_BAD_INDEX = 4,    /* index lists malformed (see sparse_attn_validate_index) */
+  SA_ERR_TIMEOUT = 5,      /* a device-side wait gave up; outputs are incomplete */
+  SA_ERR_CUDA = 6          /* a CUDA runtime call or launch failed */
+} sa_status;
+
+/* Bits a kernel ORs into the optional device status word (int32). */
+#define SA_DEVERR_ROW_PTR 1   /* row_ptr not monotone / out of [0, nnz] */
+#define SA_DEVERR_INDEX 2     /* a key index outside [0, Nk) or lists not ascending */
+#define SA_DEVERR_TIMEOUT 4   /* a bounded wait ran out */
+#define SA_DEVERR_CAPACITY 8  /* the builder's lists did not fit col_capacity */
+
+typedef enum {
+  SA_SELECT_TOPK = 0,       /* keep the topk highest-scoring keys */
+  SA_SELECT_THRESHOLD = 1,  /* keep keys whose mean-query probability >= threshold */
+  SA_SELECT_MASS = 2        /* keep the fewest top keys whose probability sum >= mass */
+} sa_select_mode;
+
+/* Element type of the attention output o. */
+#define SA_OUT_BF16 0
+#define SA_OUT_FP32 1
+
+typedef struct {
+  int32_t B, H;       /* batch, heads */
+  int32_t Nq, Nk;     /* query tokens, key/value tokens per head */
+  int32_t d;          /* head dimension: 64 or 128 */
+  int32_t group_size; /* M: contiguous queries sharing one key list (128, or C = 192) */
+  float scale;        /* softmax scale, normally 1/sqrt(d); finite, non-zero */
+  int32_t out_dtype;  /* SA_OUT_BF16 (0, default) or SA_OUT_FP32; forward only */
+} sa_problem;
+
+typedef struct {
+  int32_t mode;       /* sa_select_mode */
+  int64_t topk;       /* TOPK: number of keys, clamped to [1, Nk] */
+  double threshold;   /* THRESHOLD: tau in [0, 1] */
+  double mass;        /* MASS: rho in (0, 1] */
+} sa_select;
+
+/*
+ * Bytes of device workspace sparse_attn_build_index needs for this problem
+ * (mean queries, the fp32 score matrix of every group against every key,
+ * per-row selection results and counters).  0 if the problem is invalid.
+ */
+size_t sparse_attn_build_index_workspace_size(const sa_problem* problem);
+
+/*
+ * Builds the per-group key lists (FG-Attn review, §4.4 pooling mask; LoSA's
+ * retained-mass rule).  For each unit (b, h, g):
+ *   q_avg = mean of the group's query rows;
+ *   sigma_j = scale * (q_avg . k_j) for every key j < Nk;
+ *   keys ranked by (sigma descending, index ascending), then
+ *     TOPK:      the first min(topk, Nk) keys;
+ *     THRESHOLD: keys with p_j = exp(sigma_j - logsumexp(sigma)) >= threshold,
+ *                or the top-ranked key if none qualifies;
+ *     MASS:      the shortest ranked prefix whose sum of p_j reaches mass.
+ * Lists are written ascending into col_idx with row_ptr as their CSR offsets
+ * (row_ptr[0] = 0, row_ptr[rows] = nnz).  Scores are computed in fp32 from
+ * an fp32 mean query (split into two bf16 terms for the tensor cores), so a
+ * key whose score lies within rounding of the cut may fall either side.
+ *
+ *  q, k          device bf16 [B,H,Nq,d], [B,H,Nk,d]
+ *  row_ptr       device int64 [B*H*G + 1], written
+ *  col_idx       device int32 [col_capacity], written
+ *  col_capacity  entries available in col_idx
+ *  nnz_out_host  host int64, nullable.  If set, the call synchronises the
+ *                stream, stores nnz and reports SA_ERR_CAPACITY /
+ *                SA_ERR_TIMEOUT.  In THRESHOLD and MASS modes nnz is data
+ *                dependent: unless col_capacity >= B*H*G*Nk, nnz_out_host
+ *                must be given (else SA_ERR_INVALID_ARG).  In TOPK mode nnz
+ *                is B*H*G*min(topk,Nk) and is checked up front.
+ *  workspace     device, >= sparse_attn_build_index_workspace_size bytes;
+ *                contents on entry do not matter; must not be shared with a
+ *                concurrent call.
+ * Lists that would overflow col_capacity are not written (row_ptr still is).
+ */
+sa_status sparse_attn_build_index(const sa_problem* problem, const sa_select* select,
+                                  const void* q, const void* k, int64_t* row_ptr,
+                                  int32_t* col_idx, int64_t col_capacity,
+                                  int64_t* nnz_out_host, void* workspace,
+                                  size_t workspace_bytes, sa_stream_t stream);
+
+/*
+ * Column-sparse attention forward (FG-Attn review, "What carries the
+ * argument": gather-load of the listed K/V rows into tensor-core tiles;
+ * Chipmunk review, Alg. 3: softmax renormalised over the kept keys).
+ * For each query row i of unit u with kept keys K_u = col_idx[row_ptr[u]..):
+ *   l_ij = scale * q_i . k_j  (j in K_u),   m_i = max_j l_ij,
+ *   o_i = sum_j exp(l_ij - m_i) v_j / sum_j exp(l_ij - m_i),
+ *   lse_i = m_i + ln sum_j exp(l_ij - m_i)     (natural log).
+ * An empty list gives o_i = 0 and lse_i = -inf.  Duplicate indices count
+ * twice; order within a list does not matter.
+ *
+ *  q             device bf16 [B,H,Nq,d]
+ *  k, v          device bf16 [B,H,Nk,d]
+ *  row_ptr       device int64 [B*H*G + 1]
+ *  col_idx       device int32 [nnz]
+ *  nnz           length of col_idx; every row_ptr entry must lie in [0, nnz]
+ *  o             device [B,H,Nq,d], written: bf16 (the fp32 result rounded to
+ *                nearest even) or fp32, per problem->out_dtype
+ *  lse           device fp32 [B,H,Nq], written; nullable
+ *  dev_status    device int32, nullable.  Malformed input never makes the
+ *                kernel read out of bounds: a unit whose row_ptr pair is out
+ *                of order or outside [0, nnz] is treated as empty, and an index
+ *                outside [0, Nk) as a zero K/V row; the matching
+ *                SA_DEVERR_* bit is ORed into *dev_status (never cleared).
+ */
+sa_status sparse_attn_forward(const sa_problem* problem, const void* q, const void* k,
+                              const void* v, const int64_t* row_ptr, const int32_t* col_idx,
+                              int64_t nnz, void* o, float* lse, int32_t* dev_status,
+                              sa_stream_t stream);
+
+/*
+ * Checks index lists without trapping: row_ptr[0] == 0, row_ptr[rows] == nnz,
+ * row_ptr non-decreasing, every index in [0, Nk) and strictly ascending
+ * within its row.  dev_status is a caller-provided device int32 used as the
+ * flag word (cleared first).  Synchronises the stream.  Returns SA_OK or
+ * SA_ERR_BAD_INDEX.
+ */
+sa_status sparse_attn_validate_index(const sa_problem* problem, const int64_t* row_ptr,
+                                     const int32_t* col_idx, int64_t nnz,
+                                     int32_t* dev_status, sa_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* sparse_attn_status_string(sa_status status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int32_t sparse_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_ATTN_H */

@@ -1,0 +1,208 @@
+"""ctypes binding of ``libsparse_attn.so`` (declared in include/sparse_attn.h).
+
+Argument marshalling only: torch CUDA tensors are passed as raw device
+pointers together with ``torch.cuda.current_stream()``.  Every step of the
+path runs in the library's kernels; there is no CPU or PyTorch fallback, and
+a missing library raises at import.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsparse_attn.so")
+
+SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_CAPACITY = 0, 1, 2, 3
+SA_ERR_BAD_INDEX, SA_ERR_TIMEOUT, SA_ERR_CUDA = 4, 5, 6
+SA_DEVERR_ROW_PTR, SA_DEVERR_INDEX, SA_DEVERR_TIMEOUT, SA_DEVERR_CAPACITY = 1, 2, 4, 8
+SA_SELECT_TOPK, SA_SELECT_THRESHOLD, SA_SELECT_MASS = 0, 1, 2
+_MODES = {"topk": SA_SELECT_TOPK, "threshold": SA_SELECT_THRESHOLD, "mass": SA_SELECT_MASS}
+
+
+class SparseAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {sparse_attn_status_string(status)} (status {status})")
+
+
+class sa_problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("Nq", ctypes.c_int32),
+                ("Nk", ctypes.c_int32), ("d", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("out_dtype", ctypes.c_int32)]
+
+
+SA_OUT_BF16, SA_OUT_FP32 = 0, 1
+_OUT = {torch.bfloat16: SA_OUT_BF16, torch.float32: SA_OUT_FP32}
+
+
+class sa_select(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("topk", ctypes.c_int64),
+                ("threshold", ctypes.c_double), ("mass", ctypes.c_double)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(nvcc, sm_103a). There is no fallback implementation.")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i64, vp = ctypes.POINTER, ctypes.c_int64, ctypes.c_void_p
+    lib.sparse_attn_build_index_workspace_size.argtypes = [P(sa_problem)]
+    lib.sparse_attn_build_index_workspace_size.restype = ctypes.c_size_t
+    lib.sparse_attn_build_index.argtypes = [P(sa_problem), P(sa_select), vp, vp, vp, vp, i64,
+                                            P(ctypes.c_int64), vp, ctypes.c_size_t, vp]
+    lib.sparse_attn_build_index.restype = ctypes.c_int
+    lib.sparse_attn_forward.argtypes = [P(sa_problem), vp, vp, vp, vp, vp, i64, vp, vp, vp, vp]
+    lib.sparse_attn_forward.restype = ctypes.c_int
+    lib.sparse_attn_validate_index.argtypes = [P(sa_problem), vp, vp, i64, vp, vp]
+    lib.sparse_attn_validate_index.restype = ctypes.c_int
+    lib.sparse_attn_status_string.argtypes = [ctypes.c_int]
+    lib.sparse_attn_status_string.restype = ctypes.c_char_p
+    lib.sparse_attn_version.argtypes = []
+    lib.sparse_attn_version.restype = ctypes.c_int32
+    return lib
+
+
+lib = _load()
+
+
+def sparse_attn_status_string(status: int) -> str:
+    return lib.sparse_attn_status_string(int(status)).decode()
+
+
+def sparse_attn_version() -> int:
+    return int(lib.sparse_attn_version())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def problem(q: torch.Tensor, k: torch.Tensor, group_size: int, scale: float | None = None,
+            out_dtype=torch.bfloat16):
+    """sa_problem for bf16 [B,H,N,d] tensors."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be [B, H, N, d]")
+    B, H, Nq, d = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("k must be [B, H, Nk, d] with q's B, H and d")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out_dtype not in _OUT:
+        raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
+    return sa_problem(B, H, Nq, k.shape[2], d, group_size, scale, _OUT[out_dtype])
+
+
+def _check(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of {dtype}")
+
+
+def sparse_attn_build_index_workspace_size(p: sa_problem) -> int:
+    return int(lib.sparse_attn_build_index_workspace_size(ctypes.byref(p)))
+
+
+def sparse_attn_build_index(q: torch.Tensor, k: torch.Tensor, mode="topk", *, topk: int = 0,
+                            threshold: float = 0.0, mass: float = 0.99, group_size: int = 128,
+                            scale: float | None = None, col_capacity: int | None = None,
+                            workspace: torch.Tensor | None = None, stream=None,
+                            sync_nnz: bool | None = None):
+    """Builds CSR key lists; returns (row_ptr int64, col_idx int32, nnz).
+
+    By default the call synchronises and raises on any device-side error
+    (capacity, timeout).  ``sync_nnz=False`` keeps a TOPK call fully
+    asynchronous (nnz is then known up front).  For THRESHOLD/MASS col_idx is
+    allocated for the worst case (every key) unless col_capacity is given;
+    col_idx is returned trimmed to nnz (a view).
+    """
+    _check(q, torch.bfloat16, "q")
+    _check(k, torch.bfloat16, "k")
+    p = problem(q, k, group_size, scale)
+    G = -(-p.Nq // group_size)
+    rows = p.B * p.H * G
+    m = _MODES.get(mode, mode)
+    sel = sa_select(m, int(topk), float(threshold), float(mass))
+    dev = q.device
+    row_ptr = torch.empty(rows + 1, dtype=torch.int64, device=dev)
+    if col_capacity is None:
+        col_capacity = rows * (min(max(int(topk), 1), p.Nk) if m == SA_SELECT_TOPK else p.Nk)
+    col_idx = torch.empty(max(col_capacity, 1), dtype=torch.int32, device=dev)
+    ws_bytes = sparse_attn_build_index_workspace_size(p)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if sync_nnz is None:
+        sync_nnz = True
+    nnz = ctypes.c_int64(0)
+    st = lib.sparse_attn_build_index(ctypes.byref(p), ctypes.byref(sel), _ptr(q), _ptr(k),
+                                     _ptr(row_ptr), _ptr(col_idx), int(col_capacity),
+                                     ctypes.byref(nnz) if sync_nnz else None, _ptr(workspace),
+                                     workspace.numel(), _stream(stream))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_build_index")
+    n = nnz.value if sync_nnz else rows * min(max(int(topk), 1), p.Nk)
+    return row_ptr, col_idx[:n], n
+
+
+def sparse_attn_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch.Tensor,
+                        col_idx: torch.Tensor, *, group_size: int = 128, scale: float | None = None,
+                        nnz: int | None = None, out: torch.Tensor | None = None,
+                        out_dtype=torch.bfloat16, lse: torch.Tensor | bool = True,
+                        status: torch.Tensor | None = None, stream=None):
+    """Column-sparse attention; returns (o [B,H,Nq,d] in out_dtype (bf16 or
+    fp32; taken from `out` if given), lse fp32 [B,H,Nq] or None)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, torch.bfloat16, n)
+    _check(row_ptr, torch.int64, "row_ptr")
+    _check(col_idx, torch.int32, "col_idx")
+    if v.shape != k.shape:
+        raise ValueError("v must have k's shape")
+    if out is not None:
+        _check(out, out.dtype, "out")
+        out_dtype = out.dtype
+    p = problem(q, k, group_size, scale, out_dtype)
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if lse is True:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    elif lse is False:
+        lse = None
+    if nnz is None:
+        nnz = col_idx.numel()
+    st = lib.sparse_attn_forward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr),
+                                 _ptr(col_idx) if col_idx.numel() else None, int(nnz), _ptr(out),
+                                 _ptr(lse), _ptr(status), _stream(stream))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_forward")
+    return out, lse
+
+
+def sparse_attn_validate_index(row_ptr: torch.Tensor, col_idx: torch.Tensor, *, B: int, H: int,
+                               Nq: int, Nk: int, d: int = 128, group_size: int = 128,
+                               status: torch.Tensor | None = None, stream=None) -> int:
+    """Returns SA_OK or SA_ERR_BAD_INDEX (synchronises)."""
+    _check(row_ptr, torch.int64, "row_ptr")
+    _check(col_idx, torch.int32, "col_idx")
+    p = sa_problem(B, H, Nq, Nk, d, group_size, 1.0 / math.sqrt(d), SA_OUT_BF16)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=row_ptr.device)
+    st = lib.sparse_attn_validate_index(ctypes.byref(p), _ptr(row_ptr),
+                                        _ptr(col_idx) if col_idx.numel() else None,
+                                        col_idx.numel(), _ptr(status), _stream(stream))
+    if st not in (SA_OK, SA_ERR_BAD_INDEX):
+        raise SparseAttnError(st, "sparse_attn_validate_index")
+    return st
+
+
+# Short aliases for Python callers.
+build_index = sparse_attn_build_index
+forward = sparse_attn_forward
+validate_index = sparse_attn_validate_index

@@ -1,0 +1,257 @@
+// sa_api.cu — the C ABI (include/sparse_attn.h): argument checks, buffer
+// extent checks, workspace sizing, launch and status mapping.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "sa_internal.h"
+#include "sparse_attn.h"
+
+namespace {
+
+constexpr int32_t kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int kMaxDevices = 64;
+
+struct Dims {
+  int64_t G, rows;
+};
+
+sa_status check_problem(const sa_problem* p, Dims* dims) {
+  if (!p) return SA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || p->Nq < 1 || p->Nk < 1 || p->d < 1 || p->group_size < 1)
+    return SA_ERR_INVALID_ARG;
+  if (!std::isfinite(p->scale) || p->scale == 0.f) return SA_ERR_INVALID_ARG;
+  if (p->d != 64 && p->d != 128) return SA_ERR_UNSUPPORTED;
+  if (p->group_size > 256) return SA_ERR_UNSUPPORTED;
+  if (p->out_dtype != SA_OUT_BF16 && p->out_dtype != SA_OUT_FP32) return SA_ERR_INVALID_ARG;
+  dims->G = (int64_t(p->Nq) + p->group_size - 1) / p->group_size;
+  dims->rows = int64_t(p->B) * p->H * dims->G;
+  if (dims->rows >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;  // grid.x of the per-row kernels
+  return SA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// --------------------------------------------------------------- device info
+std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_ok[kMaxDevices];  // 0 unknown, 1 sm_103, 2 other
+
+using AddrRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+std::atomic<AddrRangeFn> g_addr_range{nullptr};
+
+sa_status device_info(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SA_ERR_UNSUPPORTED;
+  int ok = g_ok[dev].load();
+  if (ok == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaFree(nullptr) != cudaSuccess ||  // makes the primary context current
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SA_ERR_CUDA;
+    g_sms[dev].store(sms);
+    ok = (major == 10 && minor == 3) ? 1 : 2;
+    g_ok[dev].store(ok);
+  }
+  if (ok != 1) return SA_ERR_UNSUPPORTED;
+  *num_sms = g_sms[dev].load();
+  if (!g_addr_range.load()) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return SA_ERR_CUDA;
+    g_addr_range.store(reinterpret_cast<AddrRangeFn>(fn));
+  }
+  return SA_OK;
+}
+
+// [p, p + bytes) must lie inside one device allocation.  Catches host
+// pointers, freed memory and buffers too small for the stated shape before
+// any kernel could touch them.
+bool in_device_allocation(const void* p, uint64_t bytes) {
+  if (!p) return false;
+  CUdeviceptr base = 0;
+  size_t size = 0;
+  const CUdeviceptr dp = reinterpret_cast<CUdeviceptr>(p);
+  if (g_addr_range.load()(&base, &size, dp) != CUDA_SUCCESS) return false;
+  return dp >= base && bytes <= size && dp - base <= size - bytes;
+}
+
+sa_status map_cuda(cudaError_t e) { return e == cudaSuccess ? SA_OK : SA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* sparse_attn_status_string(sa_status s) {
+  switch (s) {
+    case SA_OK: return "ok";
+    case SA_ERR_INVALID_ARG: return "invalid argument";
+    case SA_ERR_UNSUPPORTED: return "unsupported problem or device";
+    case SA_ERR_CAPACITY: return "col_idx capacity too small";
+    case SA_ERR_BAD_INDEX: return "malformed index lists";
+    case SA_ERR_TIMEOUT: return "device wait timed out";
+    case SA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+int32_t sparse_attn_version(void) { return kVersion; }
+
+size_t sparse_attn_build_index_workspace_size(const sa_problem* p) {
+  Dims dims;
+  if (check_problem(p, &dims) != SA_OK) return 0;
+  return sa::build_layout(dims.rows, p->Nk, p->d).total;
+}
+
+sa_status sparse_attn_build_index(const sa_problem* p, const sa_select* sel, const void* q,
+                                  const void* k, int64_t* row_ptr, int32_t* col_idx,
+                                  int64_t col_capacity, int64_t* nnz_out_host, void* workspace,
+                                  size_t workspace_bytes, sa_stream_t stream) {
+  Dims dims;
+  sa_status st = check_problem(p, &dims);
+  if (st != SA_OK) return st;
+  if (!sel || sel->mode < SA_SELECT_TOPK || sel->mode > SA_SELECT_MASS) return SA_ERR_INVALID_ARG;
+  if (sel->mode == SA_SELECT_TOPK && sel->topk < 1) return SA_ERR_INVALID_ARG;
+  if (sel->mode == SA_SELECT_THRESHOLD && !(sel->threshold >= 0.0 && sel->threshold <= 1.0))
+    return SA_ERR_INVALID_ARG;
+  if (sel->mode == SA_SELECT_MASS && !(sel->mass > 0.0 && sel->mass <= 1.0)) return SA_ERR_INVALID_ARG;
+  if (!q || !k || !row_ptr || !workspace || col_capacity < 0) return SA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(row_ptr, 8) || !aligned(workspace, 256) ||
+      (col_idx && !aligned(col_idx, 4)))
+    return SA_ERR_INVALID_ARG;
+  const sa::BuildLayout L = sa::build_layout(dims.rows, p->Nk, p->d);
+  if (workspace_bytes < L.total) return SA_ERR_INVALID_ARG;
+  const int64_t max_nnz = dims.rows * p->Nk;
+  if (sel->mode == SA_SELECT_TOPK) {
+    const int64_t kk = sel->topk < p->Nk ? sel->topk : p->Nk;
+    if (dims.rows * kk > col_capacity) {
+      if (nnz_out_host) *nnz_out_host = dims.rows * kk;
+      return SA_ERR_CAPACITY;
+    }
+  } else if (col_capacity < max_nnz && !nnz_out_host) {
+    return SA_ERR_INVALID_ARG;  // data-dependent nnz needs the synchronous report
+  }
+  if (col_capacity > 0 && !col_idx) return SA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_info(&sms)) != SA_OK) return st;
+  const uint64_t qbytes = uint64_t(p->B) * p->H * p->Nq * p->d * 2;
+  const uint64_t kbytes = uint64_t(p->B) * p->H * p->Nk * p->d * 2;
+  if (!in_device_allocation(q, qbytes) || !in_device_allocation(k, kbytes) ||
+      !in_device_allocation(row_ptr, uint64_t(dims.rows + 1) * 8) ||
+      !in_device_allocation(workspace, L.total) ||
+      (col_capacity > 0 && !in_device_allocation(col_idx, uint64_t(col_capacity) * 4)))
+    return SA_ERR_INVALID_ARG;
+
+  sa::BuildArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  a.row_ptr = row_ptr;
+  a.col_idx = col_idx;
+  a.col_capacity = col_capacity;
+  a.ws = static_cast<uint8_t*>(workspace);
+  a.L = L;
+  a.rows = dims.rows;
+  a.G = dims.G;
+  a.BH = p->B * p->H;
+  a.Nq = p->Nq;
+  a.Nk = p->Nk;
+  a.d = p->d;
+  a.M = p->group_size;
+  a.scale = p->scale;
+  a.mode = sel->mode;
+  a.topk = sel->topk;
+  a.threshold = sel->threshold;
+  a.mass = sel->mass;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = map_cuda(sa::launch_build_index(a, sms, s))) != SA_OK) return st;
+  if (nnz_out_host) {
+    int64_t misc[2] = {0, 0};
+    if (cudaMemcpyAsync(misc, a.ws + L.misc, sizeof misc, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return SA_ERR_CUDA;
+    *nnz_out_host = misc[0];
+    const int32_t dev_status = static_cast<int32_t>(misc[1] & 0xFFFFFFFF);
+    if (dev_status & SA_DEVERR_TIMEOUT) return SA_ERR_TIMEOUT;
+    if (dev_status & SA_DEVERR_CAPACITY) return SA_ERR_CAPACITY;
+  }
+  return SA_OK;
+}
+
+sa_status sparse_attn_forward(const sa_problem* p, const void* q, const void* k, const void* v,
+                              const int64_t* row_ptr, const int32_t* col_idx, int64_t nnz,
+                              void* o, float* lse, int32_t* dev_status, sa_stream_t stream) {
+  Dims dims;
+  sa_status st = check_problem(p, &dims);
+  if (st != SA_OK) return st;
+  if (!q || !k || !v || !row_ptr || !o || nnz < 0 || (nnz > 0 && !col_idx)) return SA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(row_ptr, 8) || (col_idx && !aligned(col_idx, 4)) || (lse && !aligned(lse, 4)) ||
+      (dev_status && !aligned(dev_status, 4)))
+    return SA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_info(&sms)) != SA_OK) return st;
+  const uint64_t qbytes = uint64_t(p->B) * p->H * p->Nq * p->d * 2;
+  const uint64_t kbytes = uint64_t(p->B) * p->H * p->Nk * p->d * 2;
+  const uint64_t obytes = p->out_dtype == SA_OUT_FP32 ? 2 * qbytes : qbytes;
+  if (!in_device_allocation(q, qbytes) || !in_device_allocation(k, kbytes) ||
+      !in_device_allocation(v, kbytes) || !in_device_allocation(o, obytes) ||
+      !in_device_allocation(row_ptr, uint64_t(dims.rows + 1) * 8) ||
+      (nnz > 0 && !in_device_allocation(col_idx, uint64_t(nnz) * 4)) ||
+      (lse && !in_device_allocation(lse, uint64_t(p->B) * p->H * p->Nq * 4)) ||
+      (dev_status && !in_device_allocation(dev_status, 4)))
+    return SA_ERR_INVALID_ARG;
+  sa::FwdArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.row_ptr = row_ptr;
+  a.col_idx = col_idx;
+  a.nnz = nnz;
+  a.o = o;
+  a.out_fp32 = p->out_dtype == SA_OUT_FP32 ? 1 : 0;
+  a.lse = lse;
+  a.status = dev_status;
+  a.units = dims.rows;
+  a.G = dims.G;
+  a.Nq = p->Nq;
+  a.Nk = p->Nk;
+  a.M = p->group_size;
+  a.scale_log2 = static_cast<float>(static_cast<double>(p->scale) * 1.4426950408889634);
+  return map_cuda(sa::launch_forward(a, p->d, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sa_status sparse_attn_validate_index(const sa_problem* p, const int64_t* row_ptr,
+                                     const int32_t* col_idx, int64_t nnz, int32_t* dev_status,
+                                     sa_stream_t stream) {
+  Dims dims;
+  sa_status st = check_problem(p, &dims);
+  if (st != SA_OK) return st;
+  if (!row_ptr || !dev_status || nnz < 0 || (nnz > 0 && !col_idx)) return SA_ERR_INVALID_ARG;
+  if (!aligned(row_ptr, 8) || !aligned(dev_status, 4) || (col_idx && !aligned(col_idx, 4)))
+    return SA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_info(&sms)) != SA_OK) return st;
+  if (!in_device_allocation(row_ptr, uint64_t(dims.rows + 1) * 8) ||
+      (nnz > 0 && !in_device_allocation(col_idx, uint64_t(nnz) * 4)) ||
+      !in_device_allocation(dev_status, 4))
+    return SA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t flags = 0;
+  if (cudaMemsetAsync(dev_status, 0, 4, s) != cudaSuccess) return SA_ERR_CUDA;
+  if ((st = map_cuda(sa::launch_validate(row_ptr, col_idx, dims.rows, nnz, p->Nk, dev_status, s))) != SA_OK)
+    return st;
+  if (cudaMemcpyAsync(&flags, dev_status, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return SA_ERR_CUDA;
+  return flags ? SA_ERR_BAD_INDEX : SA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,443 @@
+// sa_forward.cu — fused column-sparse attention forward for sm_103a.
+//
+// One persistent CTA per SM walks (batch, head, group) units in head-major
+// order.  Per unit it keeps the group's queries in shared memory and streams
+// the unit's kept keys in tiles of BN:
+//   gather warps  copy the listed K and V rows (16-byte cp.async per chunk)
+//                 into 128B-swizzled tiles — the FG-Attn review's gather-load
+//                 ("What carries the argument"): indices go to registers,
+//                 addresses are formed per thread, rows land in
+//                 tensor-core-ready shared-memory tiles;
+//   the MMA warp  issues S = Q K^T (tcgen05, fp32 in TMEM, double-buffered)
+//                 and O += P V with P read from TMEM;
+//   softmax warps keep the running max / sum per query row in registers
+//                 (DiT page, "Online Softmax"), write P as bf16 over S in
+//                 TMEM and rescale O only when the row max grows by more
+//                 than 2^8 (exact after the final division by the sum);
+//                 the epilogue writes O / l in bf16 and lse = m + ln l.
+// The softmax is restricted to the kept keys (Chipmunk review, major
+// comment 1, Alg. 3).  Groups longer than 128 rows (C = 192) use two
+// 128-row blocks that share every K/V tile.
+#include "sa_device.cuh"
+#include "sa_internal.h"
+
+namespace sa {
+
+template <int D, int RB, int BN, int STAGES>
+struct FwdCfg {
+  static constexpr int kSoftmaxWarps = 4 * RB;
+  static constexpr int kMmaWarp = kSoftmaxWarps;
+  static constexpr int kProdWarp0 = kSoftmaxWarps + 1;
+  static constexpr int kProdWarps = 4;
+  static constexpr int kProdThreads = 32 * kProdWarps;
+  static constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProdWarps);
+  static constexpr int kChunks = D / 8;          // 16-byte chunks per row
+  static constexpr int kRowStep = kProdThreads / kChunks;
+  static constexpr int kKVRowsPerThread = BN / kRowStep;
+  static constexpr int kQRowsPerThread = 128 * RB / kRowStep;
+  static constexpr int kQBlock = 128 * D * 2;    // one 128-row block of Q
+  static constexpr int kQBytes = RB * kQBlock;
+  static constexpr int kTile = BN * D * 2;       // one K or V tile
+  static constexpr int kSCols = RB * BN;         // TMEM columns per S buffer
+  static constexpr int kOCol = 2 * kSCols;
+  static constexpr int kUsedCols = 2 * kSCols + RB * D;
+  static constexpr int kTmemCols = kUsedCols <= 128 ? 128 : (kUsedCols <= 256 ? 256 : 512);
+  static constexpr int kBarBytes = 1024;
+  static constexpr int kSmemBytes = 1024 + kQBytes + 2 * STAGES * kTile + kBarBytes;
+  static_assert(kUsedCols <= 512, "TMEM budget");
+  static_assert(BN % 64 == 0 && D % 64 == 0, "tile shapes");
+  static_assert(kProdThreads % kChunks == 0 && BN % kRowStep == 0, "gather mapping");
+};
+
+template <int RB, int STAGES>
+struct FwdBars {
+  uint64_t kfull[STAGES], vfull[STAGES], kempty[STAGES], vempty[STAGES];
+  uint64_t qfull, qempty, drain;
+  uint64_t sfull[2][RB], pfull[2][RB], pvdone[2][RB], ofree[RB];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Unit u's list bounds.  A malformed row_ptr pair makes the unit empty.
+__device__ __forceinline__ int64_t unit_list(const FwdArgs& a, int64_t u, int64_t* begin,
+                                             bool* bad) {
+  const int64_t b0 = __ldg(a.row_ptr + u), b1 = __ldg(a.row_ptr + u + 1);
+  if (b0 < 0 || b1 < b0 || b1 > a.nnz) {
+    *bad = true;
+    *begin = 0;
+    return 0;
+  }
+  *bad = false;
+  *begin = b0;
+  return b1 - b0;
+}
+
+template <int D, int RB, int BN, int STAGES>
+__global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
+    sa_forward_kernel(const FwdArgs a) {
+  using C = FwdCfg<D, RB, BN, STAGES>;
+  using Bars = FwdBars<RB, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + C::kQBytes;
+  uint8_t* sV = sK + STAGES * C::kTile;
+  Bars* bars = reinterpret_cast<Bars*>(sV + STAGES * C::kTile);
+  volatile int* abort = &bars->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bars->kfull[s], C::kProdThreads);
+      mbar_init(&bars->vfull[s], C::kProdThreads);
+      mbar_init(&bars->kempty[s], 1);
+      mbar_init(&bars->vempty[s], 1);
+    }
+    mbar_init(&bars->qfull, C::kProdThreads);
+    mbar_init(&bars->qempty, 1);
+    mbar_init(&bars->drain, 1);
+    for (int b = 0; b < 2; ++b)
+      for (int r = 0; r < RB; ++r) {
+        mbar_init(&bars->sfull[b][r], 1);
+        mbar_init(&bars->pfull[b][r], 128);
+        mbar_init(&bars->pvdone[b][r], 1);
+      }
+    for (int r = 0; r < RB; ++r) mbar_init(&bars->ofree[r], 128);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const int64_t G = a.G;
+
+  if (warp < C::kSoftmaxWarps) {
+    // ------------------------------------------------------------ softmax
+    const int rb = warp >> 2, quarter = warp & 3;
+    const int row_in_unit = rb * 128 + quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t t = 0, un = 0;
+    for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
+      int64_t begin;
+      bool bad;
+      const int64_t len = unit_list(a, u, &begin, &bad);
+      if (bad && threadIdx.x == 0) report(a.status, SA_DEVERR_ROW_PTR);
+      const int64_t bh = u / G, g = u % G;
+      const int64_t grow = g * a.M + row_in_unit;
+      const bool valid = row_in_unit < a.M && grow < a.Nq;
+      const int64_t orow_off = (bh * a.Nq + grow) * D;
+      const uint32_t n = static_cast<uint32_t>((len + BN - 1) / BN);
+      if (n == 0) {
+        if (valid) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          uint4* dst = a.out_fp32 ? reinterpret_cast<uint4*>(static_cast<float*>(a.o) + orow_off)
+                                  : reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + orow_off);
+          const int n16 = a.out_fp32 ? D / 4 : D / 8;
+          for (int c = 0; c < n16; ++c) dst[c] = z;
+          if (a.lse) a.lse[bh * a.Nq + grow] = -INFINITY;
+        }
+        continue;
+      }
+      float m = -INFINITY, l = 0.f, lr = 0.f;
+      for (uint32_t j = 0; j < n; ++j) {
+        const uint32_t tt = t + j, b = tt & 1;
+        const int nvalid = static_cast<int>(min64(BN, len - int64_t(j) * BN));
+        if (!mbar_wait(&bars->sfull[b][rb], (tt >> 1) & 1, abort)) goto done;
+        tc_fence_after();
+        const uint32_t sbase = tmem + lane_base + b * C::kSCols + rb * BN;
+        float x[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(sbase + c * 32, reinterpret_cast<uint32_t*>(x + c * 32));
+        tmem_ld_wait();
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          x[c] = c < nvalid ? x[c] * a.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, x[c]);
+        }
+        if (j == 0) {
+          m = mx;
+        } else if (__any_sync(0xffffffffu, mx > m + 8.f)) {
+          // O must hold PV of the previous tile before it is rescaled.
+          const uint32_t tp = tt - 1;
+          if (!mbar_wait(&bars->pvdone[tp & 1][rb], (tp >> 1) & 1, abort)) goto done;
+          tc_fence_after();
+          float alpha = 1.f;
+          if (mx > m + 8.f) {
+            alpha = fast_exp2(m - mx);
+            m = mx;
+          }
+          l *= alpha;
+          lr *= alpha;
+          const uint32_t obase = tmem + lane_base + C::kOCol + rb * D;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(obase + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(obase + c * 32, r);
+          }
+          tmem_st_wait();
+        }
+        // Two row sums: lr over the bf16-rounded P that the PV MMA consumes
+        // (normalises O with the weights actually applied to V) and l over
+        // the fp32 P (for the log-sum-exp).
+        uint32_t p[BN / 2];
+        float sum = 0.f, sum_r = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN / 2; ++c) {
+          const float p0 = fast_exp2(x[2 * c] - m), p1 = fast_exp2(x[2 * c + 1] - m);
+          p[c] = pack_bf16(p0, p1);
+          sum += p0 + p1;
+          sum_r += __uint_as_float(p[c] << 16) + __uint_as_float(p[c] & 0xFFFF0000u);
+        }
+        l += sum;
+        lr += sum_r;
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) tmem_st32(sbase + c * 32, p + c * 32);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->pfull[b][rb]);
+      }
+      {
+        const uint32_t tl = t + n - 1;
+        if (!mbar_wait(&bars->pvdone[tl & 1][rb], (tl >> 1) & 1, abort)) goto done;
+        tc_fence_after();
+        const float inv = 1.f / lr;
+        const uint32_t obase = tmem + lane_base + C::kOCol + rb * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(obase + c * 32, r);
+          tmem_ld_wait();
+          if (a.out_fp32) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * inv);
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(a.o) + orow_off + c * 32);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) dst[e] = make_uint4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+            }
+          } else {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + orow_off + c * 32);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            }
+          }
+        }
+        if (valid && a.lse) a.lse[bh * a.Nq + grow] = m * 0.69314718055994531f + __logf(l);
+        tc_fence_before();
+        mbar_arrive(&bars->ofree[rb]);
+      }
+      t += n;
+      ++un;
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_bf16(128, BN, false, false);
+      constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
+      const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      uint32_t t = 0, un = 0;
+      bool ok = true;
+      // O += P V for tile tt (first: overwrite O).
+      auto pv = [&](uint32_t tt, bool first) -> bool {
+        const uint32_t s = tt % STAGES, b = tt & 1;
+        if (!mbar_wait(&bars->vfull[s], (tt / STAGES) & 1, abort)) return false;
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb) {
+          if (!mbar_wait(&bars->pfull[b][rb], (tt >> 1) & 1, abort)) return false;
+          if (first && un > 0 && !mbar_wait(&bars->ofree[rb], (un - 1) & 1, abort)) return false;
+          tc_fence_after();
+          const uint32_t a_tmem = tmem + b * C::kSCols + rb * BN;
+          const uint32_t d_tmem = tmem + C::kOCol + rb * D;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t bdesc = sw128_desc(v_addr + s * C::kTile + kk * 2048, BN * 128, 1024);
+            mma_ts(d_tmem, a_tmem + kk * 8, bdesc, kIdescPV, (!first || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars->pvdone[b][rb]);
+        }
+        mma_commit(&bars->vempty[s]);
+        return true;
+      };
+      for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        int64_t begin;
+        bool bad;
+        const int64_t len = unit_list(a, u, &begin, &bad);
+        const uint32_t n = static_cast<uint32_t>((len + BN - 1) / BN);
+        if (n == 0) continue;
+        if (!mbar_wait(&bars->qfull, un & 1, abort)) break;
+        for (uint32_t j = 0; j < n && ok; ++j) {
+          const uint32_t tt = t + j, s = tt % STAGES, b = tt & 1;
+          if (!mbar_wait(&bars->kfull[s], (tt / STAGES) & 1, abort)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int rb = 0; rb < RB; ++rb) {
+            const uint32_t d_tmem = tmem + b * C::kSCols + rb * BN;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t adesc = sw128_desc(q_addr + rb * C::kQBlock + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024);
+              const uint64_t bdesc = sw128_desc(k_addr + s * C::kTile + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024);
+              mma_ss(d_tmem, adesc, bdesc, kIdescS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars->sfull[b][rb]);
+          }
+          mma_commit(&bars->kempty[s]);
+          if (j == n - 1) mma_commit(&bars->qempty);
+          if (j >= 1 && !pv(tt - 1, j == 1)) ok = false;
+        }
+        if (ok && !pv(t + n - 1, n == 1)) ok = false;
+        t += n;
+        ++un;
+      }
+      // Every MMA issued above must finish before TMEM is released.
+      mma_commit(&bars->drain);
+      const long long t0 = clock64();
+      while (!mbar_test(&bars->drain, 0) && clock64() - t0 < kWaitLimitCycles) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ gather
+    const int pt = threadIdx.x - C::kProdWarp0 * 32;
+    const int chunk = pt % C::kChunks;
+    const int row0 = pt / C::kChunks;
+    const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+    uint64_t* pending = nullptr;
+    // Signals the previous copy group once it has landed (at most one group
+    // stays in flight behind the newest).
+    auto retire_previous = [&]() {
+      cp_async_wait<1>();
+      if (pending) {
+        fence_proxy_async_smem();
+        mbar_arrive(pending);
+      }
+    };
+    uint32_t t = 0, un = 0;
+    bool bad_index = false;
+    int idx_cur[C::kKVRowsPerThread], idx_prev[C::kKVRowsPerThread];
+    for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
+      int64_t begin;
+      bool bad;
+      const int64_t len = unit_list(a, u, &begin, &bad);
+      const uint32_t n = static_cast<uint32_t>((len + BN - 1) / BN);
+      if (n == 0) continue;
+      const int64_t bh = u / G, g = u % G;
+      const uint16_t* kh = a.k + bh * a.Nk * D + chunk * 8;
+      const uint16_t* vh = a.v + bh * a.Nk * D + chunk * 8;
+      // Q rows of the group (zero past the group / past Nq).
+      if (un > 0 && !mbar_wait(&bars->qempty, (un - 1) & 1, abort)) goto done;
+#pragma unroll
+      for (int i = 0; i < C::kQRowsPerThread; ++i) {
+        const int r = row0 + i * C::kRowStep;
+        const int64_t grow = g * a.M + r;
+        const bool in = r < a.M && grow < a.Nq;
+        const uint16_t* src = in ? a.q + (bh * a.Nq + grow) * D + chunk * 8 : a.q;
+        cp_async16(q_addr + (r >> 7) * C::kQBlock + sw128_offset(r & 127, chunk, 128), src, in ? 16u : 0u);
+      }
+      cp_async_commit();
+      retire_previous();
+      pending = &bars->qfull;
+      for (uint32_t j = 0; j <= n; ++j) {
+        const uint32_t tt = t + j;
+        if (j < n) {
+#pragma unroll
+          for (int i = 0; i < C::kKVRowsPerThread; ++i) {
+            const int64_t pos = int64_t(j) * BN + row0 + i * C::kRowStep;
+            int idx = -1;
+            if (pos < len) {
+              idx = __ldg(a.col_idx + begin + pos);
+              if (idx < 0 || idx >= a.Nk) {
+                bad_index = true;
+                idx = -2;
+              }
+            }
+            idx_cur[i] = idx;
+          }
+          const uint32_t s = tt % STAGES;
+          if (!mbar_wait(&bars->kempty[s], ((tt / STAGES) & 1) ^ 1, abort)) goto done;
+#pragma unroll
+          for (int i = 0; i < C::kKVRowsPerThread; ++i) {
+            const int r = row0 + i * C::kRowStep;
+            const int idx = idx_cur[i];
+            const uint16_t* src = idx >= 0 ? kh + int64_t(idx) * D : a.k;
+            cp_async16(k_addr + s * C::kTile + sw128_offset(r, chunk, BN), src, idx >= 0 ? 16u : 0u);
+          }
+          cp_async_commit();
+          retire_previous();
+          pending = &bars->kfull[s];
+        }
+        if (j >= 1) {
+          const uint32_t tp = tt - 1, s = tp % STAGES;
+          if (!mbar_wait(&bars->vempty[s], ((tp / STAGES) & 1) ^ 1, abort)) goto done;
+#pragma unroll
+          for (int i = 0; i < C::kKVRowsPerThread; ++i) {
+            const int r = row0 + i * C::kRowStep;
+            const int idx = idx_prev[i];
+            const uint16_t* src = idx >= 0 ? vh + int64_t(idx) * D : a.v;
+            cp_async16(v_addr + s * C::kTile + sw128_offset(r, chunk, BN), src, idx >= 0 ? 16u : 0u);
+          }
+          cp_async_commit();
+          retire_previous();
+          pending = &bars->vfull[s];
+        }
+#pragma unroll
+        for (int i = 0; i < C::kKVRowsPerThread; ++i) idx_prev[i] = idx_cur[i];
+      }
+      t += n;
+      ++un;
+    }
+    cp_async_wait<0>();
+    if (pending) {
+      fence_proxy_async_smem();
+      mbar_arrive(pending);
+    }
+    if (bad_index) report(a.status, SA_DEVERR_INDEX);
+  }
+done:
+  if (warp >= C::kProdWarp0) cp_async_wait<0>();
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && bars->abort) report(a.status, SA_DEVERR_TIMEOUT);
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, int RB, int BN, int STAGES>
+static cudaError_t launch(const FwdArgs& a, int num_sms, cudaStream_t stream) {
+  using C = FwdCfg<D, RB, BN, STAGES>;
+  auto kern = sa_forward_kernel<D, RB, BN, STAGES>;
+  // At least half the SM's shared memory, so that one CTA owns each SM's TMEM.
+  const int smem = C::kSmemBytes > 120 * 1024 ? C::kSmemBytes : 120 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = a.units < num_sms ? a.units : num_sms;
+  kern<<<static_cast<unsigned>(grid), C::kThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_forward(const FwdArgs& a, int d, int num_sms, cudaStream_t stream) {
+  if (a.units <= 0) return cudaSuccess;
+  if (d == 128) {
+    return a.M <= 128 ? launch<128, 1, 128, 3>(a, num_sms, stream)
+                      : launch<128, 2, 64, 4>(a, num_sms, stream);
+  }
+  return a.M <= 128 ? launch<64, 1, 128, 4>(a, num_sms, stream)
+                    : launch<64, 2, 64, 4>(a, num_sms, stream);
+}
+
+}  // namespace sa

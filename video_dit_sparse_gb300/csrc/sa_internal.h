@@ -1,0 +1,63 @@
+// sa_internal.h — launch interfaces between the C ABI (sa_api.cu) and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sa {
+
+struct FwdArgs {
+  const uint16_t* q;  // bf16 bits [B,H,Nq,d]
+  const uint16_t* k;  // bf16 bits [B,H,Nk,d]
+  const uint16_t* v;
+  const int64_t* row_ptr;
+  const int32_t* col_idx;
+  int64_t nnz;
+  void* o;            // [B,H,Nq,d]: bf16 bits, or fp32 when out_fp32
+  float* lse;         // [B,H,Nq] or null
+  int32_t* status;    // device status word or null
+  int64_t units;      // B*H*G
+  int64_t G;
+  int32_t Nq, Nk, M;
+  int32_t out_fp32;
+  float scale_log2;   // scale * log2(e)
+};
+
+cudaError_t launch_forward(const FwdArgs& a, int d, int num_sms, cudaStream_t stream);
+
+// Index builder.  The workspace holds, in order (each 256-byte aligned):
+//   qhi, qlo   bf16 [rows, d]   mean query split as hi + lo
+//   scores     fp32 [rows, ld]  ld = Nk rounded up to a multiple of 4
+//   cut        uint32 [rows]    order-preserving key of the selection cut
+//   ties       int32 [rows]     keys equal to the cut that are kept
+//   counts     int64 [rows]     kept keys per row
+//   misc       int64 nnz, int32 status
+struct BuildLayout {
+  size_t qhi, qlo, scores, cut, ties, counts, misc, total;
+  int64_t ld;
+};
+BuildLayout build_layout(int64_t rows, int32_t Nk, int32_t d);
+
+struct BuildArgs {
+  const uint16_t* q;
+  const uint16_t* k;
+  int64_t* row_ptr;
+  int32_t* col_idx;
+  int64_t col_capacity;
+  uint8_t* ws;
+  BuildLayout L;
+  int64_t rows, G;
+  int32_t BH, Nq, Nk, d, M;
+  float scale;
+  int32_t mode;
+  int64_t topk;
+  double threshold, mass;
+};
+
+cudaError_t launch_build_index(const BuildArgs& a, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_validate(const int64_t* row_ptr, const int32_t* col_idx, int64_t rows,
+                            int64_t nnz, int32_t Nk, int32_t* status, cudaStream_t stream);
+
+}  // namespace sa
