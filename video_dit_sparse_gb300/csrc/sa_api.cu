@@ -224,7 +224,8 @@ sa_status sparse_attn_forward(const sa_problem* p, const void* q, const void* k,
   a.Nq = p->Nq;
   a.Nk = p->Nk;
   a.M = p->group_size;
-  a.scale_log2 = static_cast<float>(static_cast<double>(p->scale) * 1.4426950408889634);
+  a.neg_scale = p->scale < 0.f ? 1 : 0;
+  a.scale_log2 = static_cast<float>(std::fabs(static_cast<double>(p->scale)) * 1.4426950408889634);
   return map_cuda(sa::launch_forward(a, p->d, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 

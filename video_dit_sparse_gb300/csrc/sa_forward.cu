@@ -3,8 +3,9 @@
 // One persistent CTA per SM walks (batch, head, group) units in head-major
 // order.  Per unit it keeps the group's queries in shared memory and streams
 // the unit's kept keys in tiles of BN:
-//   gather warps  copy the listed K and V rows (16-byte cp.async per chunk)
-//                 into 128B-swizzled tiles — the FG-Attn review's gather-load
+//   gather warps  copy the listed K and V rows (16-byte cp.async per chunk,
+//                 completion tracked by the stage's mbarrier) into
+//                 128B-swizzled tiles — the FG-Attn review's gather-load
 //                 ("What carries the argument"): indices go to registers,
 //                 addresses are formed per thread, rows land in
 //                 tensor-core-ready shared-memory tiles;
@@ -25,28 +26,37 @@ namespace sa {
 
 template <int D, int RB, int BN, int STAGES>
 struct FwdCfg {
+  // 8 warps: 4*RB softmax warps, one MMA-issuing warp, the rest gather.
+  // (A block of 8 warps lets ptxas give each thread up to 255 registers;
+  // the 128-float S row of a softmax thread must not spill.)
   static constexpr int kSoftmaxWarps = 4 * RB;
   static constexpr int kMmaWarp = kSoftmaxWarps;
   static constexpr int kProdWarp0 = kSoftmaxWarps + 1;
-  static constexpr int kProdWarps = 4;
+  static constexpr int kProdWarps = RB == 1 ? 3 : 3;
   static constexpr int kProdThreads = 32 * kProdWarps;
   static constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProdWarps);
   static constexpr int kChunks = D / 8;          // 16-byte chunks per row
   static constexpr int kRowStep = kProdThreads / kChunks;
-  static constexpr int kKVRowsPerThread = BN / kRowStep;
-  static constexpr int kQRowsPerThread = 128 * RB / kRowStep;
+  static constexpr int kKVRowsPerThread = (BN + kRowStep - 1) / kRowStep;
+  static constexpr int kQRowsPerThread = (128 * RB + kRowStep - 1) / kRowStep;
   static constexpr int kQBlock = 128 * D * 2;    // one 128-row block of Q
   static constexpr int kQBytes = RB * kQBlock;
   static constexpr int kTile = BN * D * 2;       // one K or V tile
   static constexpr int kSCols = RB * BN;         // TMEM columns per S buffer
   static constexpr int kOCol = 2 * kSCols;
-  static constexpr int kUsedCols = 2 * kSCols + RB * D;
+  // The bf16-rounded row sum comes from an extra MMA, P x ones (N = 16),
+  // when TMEM has room for its 16 columns per row block.
+  static constexpr bool kSumMma = 2 * kSCols + RB * (D + 16) <= 512;
+  static constexpr int kSumCol = kOCol + RB * D;
+  static constexpr int kUsedCols = 2 * kSCols + RB * D + (kSumMma ? 16 * RB : 0);
   static constexpr int kTmemCols = kUsedCols <= 128 ? 128 : (kUsedCols <= 256 ? 256 : 512);
+  static constexpr int kOnesBytes = 1024;        // bf16 ones (512 B used) for the sum MMA
   static constexpr int kBarBytes = 1024;
-  static constexpr int kSmemBytes = 1024 + kQBytes + 2 * STAGES * kTile + kBarBytes;
+  static constexpr int kSmemBytes = 1024 + kQBytes + 2 * STAGES * kTile + kOnesBytes + kBarBytes;
   static_assert(kUsedCols <= 512, "TMEM budget");
   static_assert(BN % 64 == 0 && D % 64 == 0, "tile shapes");
-  static_assert(kProdThreads % kChunks == 0 && BN % kRowStep == 0, "gather mapping");
+  static_assert(kProdThreads % kChunks == 0, "gather mapping");
+  static_assert(kThreads == 256 || RB == 2, "one block of 8 warps for 128-row groups");
 };
 
 template <int RB, int STAGES>
@@ -82,10 +92,16 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + C::kQBytes;
   uint8_t* sV = sK + STAGES * C::kTile;
-  Bars* bars = reinterpret_cast<Bars*>(sV + STAGES * C::kTile);
+  uint8_t* sOnes = sV + STAGES * C::kTile;
+  Bars* bars = reinterpret_cast<Bars*>(sOnes + C::kOnesBytes);
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (C::kSumMma && threadIdx.x < 32) {
+    // 512 bytes of bf16 1.0, read by the tensor core through the async proxy
+    reinterpret_cast<uint4*>(sOnes)[threadIdx.x] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars->kfull[s], C::kProdThreads);
@@ -143,6 +159,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         }
         continue;
       }
+      const float sl = a.scale_log2;  // |scale| * log2(e) > 0
       float m = -INFINITY, l = 0.f, lr = 0.f;
       for (uint32_t j = 0; j < n; ++j) {
         const uint32_t tt = t + j, b = tt & 1;
@@ -154,12 +171,27 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) tmem_ld32(sbase + c * 32, reinterpret_cast<uint32_t*>(x + c * 32));
         tmem_ld_wait();
-        float mx = -INFINITY;
+        if (a.neg_scale) {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          x[c] = c < nvalid ? x[c] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x[c]);
+          for (int c = 0; c < BN; ++c) x[c] = -x[c];
         }
+        if (nvalid < BN) {  // tail tile: columns past the list do not exist
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c >= nvalid) x[c] = -INFINITY;
+        }
+        // Row max of the raw scores (scale > 0 commutes with max), 8 chains.
+        float mx;
+        {
+          float t8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t8[i] = x[i];
+#pragma unroll
+          for (int c = 8; c < BN; ++c) t8[c & 7] = fmaxf(t8[c & 7], x[c]);
+          mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
+                     fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+        }
+        mx *= sl;
         if (j == 0) {
           m = mx;
         } else if (__any_sync(0xffffffffu, mx > m + 8.f)) {
@@ -184,22 +216,32 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
             tmem_st32(obase + c * 32, r);
           }
+          if (C::kSumMma) {
+            const uint32_t saddr = tmem + lane_base + C::kSumCol + rb * 16;
+            const float sv = __uint_as_float(tmem_ld1(saddr)) * alpha;
+            tmem_st1(saddr, __float_as_uint(sv));
+          }
           tmem_st_wait();
         }
-        // Two row sums: lr over the bf16-rounded P that the PV MMA consumes
-        // (normalises O with the weights actually applied to V) and l over
-        // the fp32 P (for the log-sum-exp).
+        // P = exp2(s*x - m): one FFMA + EX2 per element.  The fp32 row sum
+        // (8 chains) feeds the log-sum-exp; O is normalised by the sum of
+        // the bf16-rounded P that the PV MMA consumes (an extra MMA against
+        // a ones tile, or here on the ALU when TMEM has no room for it).
+        const float nm = -m;
         uint32_t p[BN / 2];
-        float sum = 0.f, sum_r = 0.f;
+        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float pr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < BN / 2; ++c) {
-          const float p0 = fast_exp2(x[2 * c] - m), p1 = fast_exp2(x[2 * c + 1] - m);
+          const float p0 = fast_exp2(fmaf(x[2 * c], sl, nm));
+          const float p1 = fast_exp2(fmaf(x[2 * c + 1], sl, nm));
           p[c] = pack_bf16(p0, p1);
-          sum += p0 + p1;
-          sum_r += __uint_as_float(p[c] << 16) + __uint_as_float(p[c] & 0xFFFF0000u);
+          ps[c & 7] += p0 + p1;
+          if (!C::kSumMma)
+            pr[c & 7] += __uint_as_float(p[c] << 16) + __uint_as_float(p[c] & 0xFFFF0000u);
         }
-        l += sum;
-        lr += sum_r;
+        l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        if (!C::kSumMma) lr += ((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7]));
 #pragma unroll
         for (int c = 0; c < BN / 64; ++c) tmem_st32(sbase + c * 32, p + c * 32);
         tmem_st_wait();
@@ -210,6 +252,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         const uint32_t tl = t + n - 1;
         if (!mbar_wait(&bars->pvdone[tl & 1][rb], (tl >> 1) & 1, abort)) goto done;
         tc_fence_after();
+        if (C::kSumMma) lr = __uint_as_float(tmem_ld1(tmem + lane_base + C::kSumCol + rb * 16));
         const float inv = 1.f / lr;
         const uint32_t obase = tmem + lane_base + C::kOCol + rb * D;
 #pragma unroll
@@ -249,13 +292,17 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16(128, BN, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
+      constexpr uint32_t kIdescSum = idesc_bf16(128, 16, false, false);
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      // 16 x 16 ones, no swizzle: 8x16-byte core matrices, 128 B / 256 B apart
+      const uint64_t ones_desc = plain_desc(smem_u32(sOnes), 128, 256);
       uint32_t t = 0, un = 0;
       bool ok = true;
       // O += P V for tile tt (first: overwrite O).
       auto pv = [&](uint32_t tt, bool first) -> bool {
         const uint32_t s = tt % STAGES, b = tt & 1;
         if (!mbar_wait(&bars->vfull[s], (tt / STAGES) & 1, abort)) return false;
+        fence_proxy_async_smem();  // the V rows were written through the generic proxy
 #pragma unroll
         for (int rb = 0; rb < RB; ++rb) {
           if (!mbar_wait(&bars->pfull[b][rb], (tt >> 1) & 1, abort)) return false;
@@ -267,6 +314,13 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           for (int kk = 0; kk < BN / 16; ++kk) {
             const uint64_t bdesc = sw128_desc(v_addr + s * C::kTile + kk * 2048, BN * 128, 1024);
             mma_ts(d_tmem, a_tmem + kk * 8, bdesc, kIdescPV, (!first || kk > 0) ? 1u : 0u);
+          }
+          if (C::kSumMma) {
+            // row sums of the bf16 P: P x ones, accumulated like O
+            const uint32_t d_sum = tmem + C::kSumCol + rb * 16;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts(d_sum, a_tmem + kk * 8, ones_desc, kIdescSum, (!first || kk > 0) ? 1u : 0u);
           }
           mma_commit(&bars->pvdone[b][rb]);
         }
@@ -280,9 +334,11 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         const uint32_t n = static_cast<uint32_t>((len + BN - 1) / BN);
         if (n == 0) continue;
         if (!mbar_wait(&bars->qfull, un & 1, abort)) break;
+        fence_proxy_async_smem();
         for (uint32_t j = 0; j < n && ok; ++j) {
           const uint32_t tt = t + j, s = tt % STAGES, b = tt & 1;
           if (!mbar_wait(&bars->kfull[s], (tt / STAGES) & 1, abort)) { ok = false; break; }
+          fence_proxy_async_smem();
           tc_fence_after();
 #pragma unroll
           for (int rb = 0; rb < RB; ++rb) {
@@ -315,19 +371,15 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     const int chunk = pt % C::kChunks;
     const int row0 = pt / C::kChunks;
     const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-    uint64_t* pending = nullptr;
-    // Signals the previous copy group once it has landed (at most one group
-    // stays in flight behind the newest).
-    auto retire_previous = [&]() {
-      cp_async_wait<1>();
-      if (pending) {
-        fence_proxy_async_smem();
-        mbar_arrive(pending);
-      }
-    };
+    // Copies never block the gather warps: each stage's group completes its
+    // "full" barrier by itself (cp.async.mbarrier.arrive.noinc), and the
+    // next tile's indices are loaded while the current tile is issued, so
+    // up to STAGES tiles of K and V are in flight.
     uint32_t t = 0, un = 0;
     bool bad_index = false;
-    int idx_cur[C::kKVRowsPerThread], idx_prev[C::kKVRowsPerThread];
+    int idx_cur[C::kKVRowsPerThread], idx_nxt[C::kKVRowsPerThread], idx_prv[C::kKVRowsPerThread];
+#pragma unroll
+    for (int i = 0; i < C::kKVRowsPerThread; ++i) idx_cur[i] = idx_nxt[i] = idx_prv[i] = -1;
     for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
       int64_t begin;
       bool bad;
@@ -337,47 +389,50 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
       const int64_t bh = u / G, g = u % G;
       const uint16_t* kh = a.k + bh * a.Nk * D + chunk * 8;
       const uint16_t* vh = a.v + bh * a.Nk * D + chunk * 8;
+      // index of row r of tile jj, -1 past the list, -2 when out of range
+      auto list_index = [&](uint32_t jj, int i) -> int {
+        const int r = row0 + i * C::kRowStep;
+        const int64_t pos = int64_t(jj) * BN + r;
+        if (r >= BN || pos >= len) return -1;
+        const int idx = __ldg(a.col_idx + begin + pos);
+        if (idx < 0 || idx >= a.Nk) {
+          bad_index = true;
+          return -2;
+        }
+        return idx;
+      };
+#pragma unroll
+      for (int i = 0; i < C::kKVRowsPerThread; ++i) idx_cur[i] = list_index(0, i);
       // Q rows of the group (zero past the group / past Nq).
       if (un > 0 && !mbar_wait(&bars->qempty, (un - 1) & 1, abort)) goto done;
 #pragma unroll
       for (int i = 0; i < C::kQRowsPerThread; ++i) {
         const int r = row0 + i * C::kRowStep;
+        if (r >= 128 * RB) break;
         const int64_t grow = g * a.M + r;
         const bool in = r < a.M && grow < a.Nq;
         const uint16_t* src = in ? a.q + (bh * a.Nq + grow) * D + chunk * 8 : a.q;
         cp_async16(q_addr + (r >> 7) * C::kQBlock + sw128_offset(r & 127, chunk, 128), src, in ? 16u : 0u);
       }
-      cp_async_commit();
-      retire_previous();
-      pending = &bars->qfull;
+      cp_async_arrive_noinc(&bars->qfull);
       for (uint32_t j = 0; j <= n; ++j) {
         const uint32_t tt = t + j;
         if (j < n) {
+          if (j + 1 < n) {
 #pragma unroll
-          for (int i = 0; i < C::kKVRowsPerThread; ++i) {
-            const int64_t pos = int64_t(j) * BN + row0 + i * C::kRowStep;
-            int idx = -1;
-            if (pos < len) {
-              idx = __ldg(a.col_idx + begin + pos);
-              if (idx < 0 || idx >= a.Nk) {
-                bad_index = true;
-                idx = -2;
-              }
-            }
-            idx_cur[i] = idx;
+            for (int i = 0; i < C::kKVRowsPerThread; ++i) idx_nxt[i] = list_index(j + 1, i);
           }
           const uint32_t s = tt % STAGES;
           if (!mbar_wait(&bars->kempty[s], ((tt / STAGES) & 1) ^ 1, abort)) goto done;
 #pragma unroll
           for (int i = 0; i < C::kKVRowsPerThread; ++i) {
             const int r = row0 + i * C::kRowStep;
+            if (r >= BN) break;
             const int idx = idx_cur[i];
             const uint16_t* src = idx >= 0 ? kh + int64_t(idx) * D : a.k;
             cp_async16(k_addr + s * C::kTile + sw128_offset(r, chunk, BN), src, idx >= 0 ? 16u : 0u);
           }
-          cp_async_commit();
-          retire_previous();
-          pending = &bars->kfull[s];
+          cp_async_arrive_noinc(&bars->kfull[s]);
         }
         if (j >= 1) {
           const uint32_t tp = tt - 1, s = tp % STAGES;
@@ -385,25 +440,23 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < C::kKVRowsPerThread; ++i) {
             const int r = row0 + i * C::kRowStep;
-            const int idx = idx_prev[i];
+            if (r >= BN) break;
+            const int idx = idx_prv[i];
             const uint16_t* src = idx >= 0 ? vh + int64_t(idx) * D : a.v;
             cp_async16(v_addr + s * C::kTile + sw128_offset(r, chunk, BN), src, idx >= 0 ? 16u : 0u);
           }
-          cp_async_commit();
-          retire_previous();
-          pending = &bars->vfull[s];
+          cp_async_arrive_noinc(&bars->vfull[s]);
         }
 #pragma unroll
-        for (int i = 0; i < C::kKVRowsPerThread; ++i) idx_prev[i] = idx_cur[i];
+        for (int i = 0; i < C::kKVRowsPerThread; ++i) {
+          idx_prv[i] = idx_cur[i];
+          idx_cur[i] = idx_nxt[i];
+        }
       }
       t += n;
       ++un;
     }
     cp_async_wait<0>();
-    if (pending) {
-      fence_proxy_async_smem();
-      mbar_arrive(pending);
-    }
     if (bad_index) report(a.status, SA_DEVERR_INDEX);
   }
 done:
@@ -412,6 +465,7 @@ done:
   __syncthreads();
   if (threadIdx.x == 0 && bars->abort) report(a.status, SA_DEVERR_TIMEOUT);
   if (warp == C::kMmaWarp) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

@@ -21,7 +21,8 @@ struct FwdArgs {
   int64_t G;
   int32_t Nq, Nk, M;
   int32_t out_fp32;
-  float scale_log2;   // scale * log2(e)
+  int32_t neg_scale;  // scale < 0: scores are negated and scale_log2 = |scale| log2(e)
+  float scale_log2;   // |scale| * log2(e)
 };
 
 cudaError_t launch_forward(const FwdArgs& a, int d, int num_sms, cudaStream_t stream);
