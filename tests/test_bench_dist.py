@@ -1,0 +1,52 @@
+"""The benchmark's multi-rank path on CPU: world size 2 over gloo.  Each
+rank runs the whole layer on its own GPU in the real benchmark (heads are
+independent: no data exchange); the only collective is the max-over-ranks
+step time and the sum of the work, checked here without a GPU."""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    assert bench.dist_info() == (world, rank, rank)
+    ms, units = bench.aggregate(1.0 + rank, 100.0 * (rank + 1), world)
+    q.put((rank, ms, units))
+    dist.destroy_process_group()
+
+
+def test_aggregate_world2_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    for rank, ms, units in got:
+        assert ms == 2.0  # slowest rank
+        assert units == 300.0  # work of both ranks
+
+
+def test_kept_pairs_counts_ragged_groups():
+    import numpy as np
+    import bench
+    # 2 heads, Nq = 300, M = 128 -> groups of 128, 128, 44 rows
+    counts = np.array([5, 6, 7, 1, 2, 3])
+    row_ptr = np.concatenate([[0], np.cumsum(counts)])
+    assert bench.kept_pairs(row_ptr, 1, 2, 300, 128) == 128 * (5 + 6 + 1 + 2) + 44 * (7 + 3)
