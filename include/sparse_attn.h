@@ -135,6 +135,31 @@ sa_status sparse_attn_build_index(const sa_problem* problem, const sa_select* se
                                   size_t workspace_bytes, sa_stream_t stream);
 
 /*
+ * The index builder for callers that cannot allocate device memory.  The
+ * paper has no counterpart: this entry point exists for callers such as
+ * runtimes that forbid allocation after start-up, allocator hooks, or plugins
+ * that are handed tensor pointers but no allocator.
+ *
+ * Same operation, arguments, results and errors as sparse_attn_build_index,
+ * without the workspace: the builder's scratch lives in one library-owned
+ * device array of SA_NOALLOC_WORKSPACE_BYTES (32 MiB), which every GPU that
+ * loads this code holds until the process exits.  A problem whose
+ * sparse_attn_build_index_workspace_size exceeds that returns
+ * SA_ERR_UNSUPPORTED before anything is enqueued.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.
+ * Every call shares the array and leaves its contents behind: calls that
+ * overlap on the GPU (other streams, other host threads) race on it and must
+ * be serialised by the caller.  Calls no allocating function.
+ */
+#define SA_NOALLOC_WORKSPACE_BYTES (32u << 20)
+
+sa_status sparse_attn_build_index_noalloc(const sa_problem* problem, const sa_select* select,
+                                          const void* q, const void* k, int64_t* row_ptr,
+                                          int32_t* col_idx, int64_t col_capacity,
+                                          int64_t* nnz_out_host, sa_stream_t stream);
+
+/*
  * Column-sparse attention forward (FG-Attn review, "What carries the
  * argument": gather-load of the listed K/V rows into tensor-core tiles;
  * Chipmunk review, Alg. 3: softmax renormalised over the kept keys).
