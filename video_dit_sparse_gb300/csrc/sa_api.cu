@@ -30,6 +30,9 @@ sa_status check_problem(const sa_problem* p, Dims* dims) {
   dims->G = (int64_t(p->Nq) + p->group_size - 1) / p->group_size;
   dims->rows = int64_t(p->B) * p->H * dims->G;
   if (dims->rows >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;  // grid.x of the per-row kernels
+  // TMA row coordinates are 32-bit: all query rows and all key rows of the batch
+  const int64_t bh = int64_t(p->B) * p->H;
+  if (bh * p->Nq >= (int64_t(1) << 31) || bh * p->Nk >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;
   return SA_OK;
 }
 

@@ -6,6 +6,7 @@
 //   2. sa_score_kernel   sigma = scale * K q_avg on tcgen05 tensor cores:
 //                        A = 128 keys x d, B = 128 groups x d (hi, then lo,
 //                        accumulated), fp32 in TMEM; written [rows, Nk].
+//                        K and mean-query tiles arrive by 2-D TMA.
 //   3. sa_select_kernel  per row: the selection cut as an exact fp32 value
 //                        (3-level radix descent over order-preserving keys)
 //                        plus how many keys equal to the cut are kept.
@@ -13,6 +14,7 @@
 //   5. sa_emit_kernel    ascending indices of kept keys into col_idx.
 #include "sa_device.cuh"
 #include "sa_internal.h"
+#include "sa_tma.h"
 
 namespace sa {
 
@@ -117,11 +119,7 @@ struct ScoreArgs {
 template <int D>
 struct ScoreCfg {
   static constexpr int kStages = 4;
-  static constexpr int kProdThreads = 128;
-  static constexpr int kThreads = 32 * 9;  // 4 epilogue, 1 MMA, 4 gather warps
-  static constexpr int kChunks = D / 8;
-  static constexpr int kRowStep = kProdThreads / kChunks;
-  static constexpr int kRowsPerThread = 128 / kRowStep;
+  static constexpr int kThreads = 32 * 6;  // 4 epilogue warps, 1 MMA warp, 1 TMA warp
   static constexpr int kTile = 128 * D * 2;  // 128 rows of d bf16
   static constexpr int kSmemBytes = 1024 + 2 * kTile + kStages * kTile + 1024;
   static constexpr int kTmemCols = 256;
@@ -147,7 +145,9 @@ __device__ __forceinline__ void score_unit(const ScoreArgs& a, int64_t u, int64_
 }
 
 template <int D>
-__global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1) sa_score_kernel(const ScoreArgs a) {
+__global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1)
+    sa_score_kernel(const ScoreArgs a, const __grid_constant__ CUtensorMap tm_qhi,
+                    const __grid_constant__ CUtensorMap tm_qlo, const __grid_constant__ CUtensorMap tm_k) {
   using C = ScoreCfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -160,10 +160,10 @@ __global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1) sa_score_kernel(cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&bars->kfull[s], C::kProdThreads);
+      mbar_init(&bars->kfull[s], 1);
       mbar_init(&bars->kempty[s], 1);
     }
-    mbar_init(&bars->qfull, C::kProdThreads);
+    mbar_init(&bars->qfull, 1);
     mbar_init(&bars->qempty, 1);
     mbar_init(&bars->drain, 1);
     for (int b = 0; b < 2; ++b) {
@@ -258,19 +258,9 @@ __global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1) sa_score_kernel(cons
       while (!mbar_test(&bars->drain, 0) && clock64() - c0 < kWaitLimitCycles) {
       }
     }
-  } else {
-    // ------------------------------------------------------------ loads
-    const int pt = threadIdx.x - 5 * 32;
-    const int chunk = pt % C::kChunks, row0 = pt / C::kChunks;
+  } else if (lane == 0) {
+    // ------------------------------------------------------------ loads (TMA)
     const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl), kb = smem_u32(sK);
-    uint64_t* pending = nullptr;
-    auto retire_previous = [&]() {
-      cp_async_wait<1>();
-      if (pending) {
-        fence_proxy_async_smem();
-        mbar_arrive(pending);
-      }
-    };
     uint32_t t = 0, un = 0;
     for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
       int64_t bh;
@@ -278,49 +268,28 @@ __global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1) sa_score_kernel(cons
       score_unit(a, u, &bh, &gc, &t0, &t1);
       if (t1 <= t0) continue;
       if (un > 0 && !mbar_wait(&bars->qempty, (un - 1) & 1, abort)) goto done;
-      const int64_t g0 = int64_t(gc) * 128;
+      // mean-query rows bh*G + g0 .. +127 (rows of the next head or past the
+      // end only feed columns that are never written)
+      const int qrow = static_cast<int>(bh * a.G + int64_t(gc) * 128);
+      mbar_expect_tx(&bars->qfull, 2 * C::kTile);
 #pragma unroll
-      for (int i = 0; i < C::kRowsPerThread; ++i) {
-        const int r = row0 + i * C::kRowStep;
-        const bool in = g0 + r < a.G;
-        const int64_t off = (bh * a.G + g0 + r) * D + chunk * 8;
-        cp_async16(qh + sw128_offset(r, chunk, 128), in ? a.qhi + off : a.qhi, in ? 16u : 0u);
-        cp_async16(ql + sw128_offset(r, chunk, 128), in ? a.qlo + off : a.qlo, in ? 16u : 0u);
+      for (int cb = 0; cb < D / 64; ++cb) {
+        tma_load_2d(qh + cb * 128 * 128, &tm_qhi, 64 * cb, qrow, &bars->qfull);
+        tma_load_2d(ql + cb * 128 * 128, &tm_qlo, 64 * cb, qrow, &bars->qfull);
       }
-      cp_async_commit();
-      retire_previous();
-      pending = &bars->qfull;
-      const uint16_t* kh = a.k + bh * a.Nk * D + chunk * 8;
       for (int tile = t0; tile < t1; ++tile, ++t) {
         const uint32_t s = t % S;
         if (!mbar_wait(&bars->kempty[s], ((t / S) & 1) ^ 1, abort)) goto done;
+        mbar_expect_tx(&bars->kfull[s], C::kTile);
+        const int krow = static_cast<int>(bh * a.Nk + int64_t(tile) * 128);
 #pragma unroll
-        for (int i = 0; i < C::kRowsPerThread; ++i) {
-          const int r = row0 + i * C::kRowStep;
-          const int64_t key = int64_t(tile) * 128 + r;
-          const bool in = key < a.Nk;
-          cp_async16(kb + s * C::kTile + sw128_offset(r, chunk, 128), in ? kh + key * D : a.k, in ? 16u : 0u);
-        }
-        cp_async_commit();
-        retire_previous();
-        pending = &bars->kfull[s];
+        for (int cb = 0; cb < D / 64; ++cb)
+          tma_load_2d(kb + s * C::kTile + cb * 128 * 128, &tm_k, 64 * cb, krow, &bars->kfull[s]);
       }
-      // The unit's last K tile must be signalled before the next unit waits
-      // for qempty, which the MMA can only commit after consuming that tile.
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(pending);
-      pending = nullptr;
       ++un;
-    }
-    cp_async_wait<0>();
-    if (pending) {
-      fence_proxy_async_smem();
-      mbar_arrive(pending);
     }
   }
 done:
-  if (warp >= 5) cp_async_wait<0>();
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && bars->abort) report(a.status, SA_DEVERR_TIMEOUT);
@@ -679,11 +648,16 @@ static cudaError_t launch_scores(const BuildArgs& a, int num_sms, cudaStream_t s
   s.units = base * s.ksplit;
   s.scale = a.scale;
   s.status = status;
+  CUtensorMap tm_qhi, tm_qlo, tm_k;
+  if (!make_rows_map(&tm_qhi, s.qhi, uint64_t(a.rows), D, 128) ||
+      !make_rows_map(&tm_qlo, s.qlo, uint64_t(a.rows), D, 128) ||
+      !make_rows_map(&tm_k, a.k, uint64_t(a.BH) * a.Nk, D, 128))
+    return cudaErrorInvalidValue;
   auto kern = sa_score_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t grid = s.units < num_sms ? s.units : num_sms;
-  kern<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, st>>>(s);
+  kern<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, st>>>(s, tm_qhi, tm_qlo, tm_k);
   return cudaGetLastError();
 }
 

@@ -3,42 +3,49 @@
 // One persistent CTA per SM walks (batch, head, group) units in head-major
 // order.  Per unit it keeps the group's queries in shared memory and streams
 // the unit's kept keys in tiles of BN:
-//   gather warps  copy the listed K and V rows (16-byte cp.async per chunk,
-//                 completion tracked by the stage's mbarrier) into
+//   gather warps  copy the listed K and V rows (16-byte cp.async per chunk;
+//                 each stage's mbarrier completes when the copies land) into
 //                 128B-swizzled tiles — the FG-Attn review's gather-load
-//                 ("What carries the argument"): indices go to registers,
-//                 addresses are formed per thread, rows land in
-//                 tensor-core-ready shared-memory tiles;
+//                 (What carries the argument): the next tile's indices are
+//                 loaded into registers while this tile's copies are issued,
+//                 and rows land in tensor-core-ready shared-memory tiles.
+//                 The query tile arrives by one 2-D TMA load per 64 columns;
 //   the MMA warp  issues S = Q K^T (tcgen05, fp32 in TMEM, double-buffered)
 //                 and O += P V with P read from TMEM;
 //   softmax warps keep the running max / sum per query row in registers
 //                 (DiT page, "Online Softmax"), write P as bf16 over S in
 //                 TMEM and rescale O only when the row max grows by more
-//                 than 2^8 (exact after the final division by the sum);
+//                 than 2^32 (exact after the final division by the sum);
 //                 the epilogue writes O / l in bf16 and lse = m + ln l.
 // The softmax is restricted to the kept keys (Chipmunk review, major
 // comment 1, Alg. 3).  Groups longer than 128 rows (C = 192) use two
 // 128-row blocks that share every K/V tile.
 #include "sa_device.cuh"
 #include "sa_internal.h"
+#include "sa_tma.h"
 
 namespace sa {
 
 template <int D, int RB, int BN, int STAGES>
 struct FwdCfg {
-  // 8 warps: 4*RB softmax warps, one MMA-issuing warp, the rest gather.
-  // (A block of 8 warps lets ptxas give each thread up to 255 registers;
-  // the 128-float S row of a softmax thread must not spill.)
+  // 4*RB softmax warps, one MMA-issuing warp, three gather warps.  (A block
+  // of at most 8 warps lets ptxas give a thread up to 255 registers: the
+  // 128-float S row of a softmax thread must not spill.)
   static constexpr int kSoftmaxWarps = 4 * RB;
   static constexpr int kMmaWarp = kSoftmaxWarps;
   static constexpr int kProdWarp0 = kSoftmaxWarps + 1;
-  static constexpr int kProdWarps = RB == 1 ? 3 : 3;
+  static constexpr int kProdWarps = 3;
   static constexpr int kProdThreads = 32 * kProdWarps;
   static constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProdWarps);
-  static constexpr int kChunks = D / 8;          // 16-byte chunks per row
-  static constexpr int kRowStep = kProdThreads / kChunks;
+  // Gather mapping: 8 lanes per row, lane copies 16-byte chunks sub, sub+8
+  // (one 128-byte line of 4 rows per copy instruction).
+  static constexpr int kLanesPerRow = 8;
+  static constexpr int kChunksPerLane = (D / 8) / kLanesPerRow;
+  static constexpr int kRowStep = kProdThreads / kLanesPerRow;
   static constexpr int kKVRowsPerThread = (BN + kRowStep - 1) / kRowStep;
-  static constexpr int kQRowsPerThread = (128 * RB + kRowStep - 1) / kRowStep;
+  // Lazy rescale: O and the row sums are rescaled only when the row max
+  // grows by more than 2^kRescaleLog2.  P stays <= 2^32 and O, l within fp32.
+  static constexpr float kRescaleLog2 = 32.f;
   static constexpr int kQBlock = 128 * D * 2;    // one 128-row block of Q
   static constexpr int kQBytes = RB * kQBlock;
   static constexpr int kTile = BN * D * 2;       // one K or V tile
@@ -55,8 +62,7 @@ struct FwdCfg {
   static constexpr int kSmemBytes = 1024 + kQBytes + 2 * STAGES * kTile + kOnesBytes + kBarBytes;
   static_assert(kUsedCols <= 512, "TMEM budget");
   static_assert(BN % 64 == 0 && D % 64 == 0, "tile shapes");
-  static_assert(kProdThreads % kChunks == 0, "gather mapping");
-  static_assert(kThreads == 256 || RB == 2, "one block of 8 warps for 128-row groups");
+  static_assert(kProdThreads % kLanesPerRow == 0 && kChunksPerLane >= 1, "gather mapping");
 };
 
 template <int RB, int STAGES>
@@ -84,7 +90,7 @@ __device__ __forceinline__ int64_t unit_list(const FwdArgs& a, int64_t u, int64_
 
 template <int D, int RB, int BN, int STAGES>
 __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
-    sa_forward_kernel(const FwdArgs a) {
+    sa_forward_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq) {
   using C = FwdCfg<D, RB, BN, STAGES>;
   using Bars = FwdBars<RB, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -109,7 +115,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
       mbar_init(&bars->kempty[s], 1);
       mbar_init(&bars->vempty[s], 1);
     }
-    mbar_init(&bars->qfull, C::kProdThreads);
+    mbar_init(&bars->qfull, 1);
     mbar_init(&bars->qempty, 1);
     mbar_init(&bars->drain, 1);
     for (int b = 0; b < 2; ++b)
@@ -194,13 +200,13 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         mx *= sl;
         if (j == 0) {
           m = mx;
-        } else if (__any_sync(0xffffffffu, mx > m + 8.f)) {
+        } else if (__any_sync(0xffffffffu, mx > m + C::kRescaleLog2)) {
           // O must hold PV of the previous tile before it is rescaled.
           const uint32_t tp = tt - 1;
           if (!mbar_wait(&bars->pvdone[tp & 1][rb], (tp >> 1) & 1, abort)) goto done;
           tc_fence_after();
           float alpha = 1.f;
-          if (mx > m + 8.f) {
+          if (mx > m + C::kRescaleLog2) {
             alpha = fast_exp2(m - mx);
             m = mx;
           }
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
       auto pv = [&](uint32_t tt, bool first) -> bool {
         const uint32_t s = tt % STAGES, b = tt & 1;
         if (!mbar_wait(&bars->vfull[s], (tt / STAGES) & 1, abort)) return false;
-        fence_proxy_async_smem();  // the V rows were written through the generic proxy
+        fence_proxy_async_smem();  // V rows were written through the generic proxy
 #pragma unroll
         for (int rb = 0; rb < RB; ++rb) {
           if (!mbar_wait(&bars->pfull[b][rb], (tt >> 1) & 1, abort)) return false;
@@ -334,11 +340,10 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         const uint32_t n = static_cast<uint32_t>((len + BN - 1) / BN);
         if (n == 0) continue;
         if (!mbar_wait(&bars->qfull, un & 1, abort)) break;
-        fence_proxy_async_smem();
         for (uint32_t j = 0; j < n && ok; ++j) {
           const uint32_t tt = t + j, s = tt % STAGES, b = tt & 1;
           if (!mbar_wait(&bars->kfull[s], (tt / STAGES) & 1, abort)) { ok = false; break; }
-          fence_proxy_async_smem();
+          fence_proxy_async_smem();  // K rows were written through the generic proxy
           tc_fence_after();
 #pragma unroll
           for (int rb = 0; rb < RB; ++rb) {
@@ -367,19 +372,21 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ gather
+    // Thread pt copies 16-byte chunks (pt mod 8) + 8c of tile rows pt/8, +12, ...
+    // Copies never block the gather warps: each stage's "full" barrier is
+    // completed by the copies themselves (cp.async.mbarrier.arrive.noinc).
+    // The next tile's indices are loaded while this tile's copies are issued
+    // and are not inspected before their own tile, so their latency hides
+    // behind a whole tile of work.
     const int pt = threadIdx.x - C::kProdWarp0 * 32;
-    const int chunk = pt % C::kChunks;
-    const int row0 = pt / C::kChunks;
+    const int sub = pt % C::kLanesPerRow;
+    const int row0 = pt / C::kLanesPerRow;
     const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-    // Copies never block the gather warps: each stage's group completes its
-    // "full" barrier by itself (cp.async.mbarrier.arrive.noinc), and the
-    // next tile's indices are loaded while the current tile is issued, so
-    // up to STAGES tiles of K and V are in flight.
     uint32_t t = 0, un = 0;
     bool bad_index = false;
     int idx_cur[C::kKVRowsPerThread], idx_nxt[C::kKVRowsPerThread], idx_prv[C::kKVRowsPerThread];
 #pragma unroll
-    for (int i = 0; i < C::kKVRowsPerThread; ++i) idx_cur[i] = idx_nxt[i] = idx_prv[i] = -1;
+    for (int i = 0; i < C::kKVRowsPerThread; ++i) idx_cur[i] = idx_nxt[i] = idx_prv[i] = 0;
     for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
       int64_t begin;
       bool bad;
@@ -387,64 +394,60 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
       const uint32_t n = static_cast<uint32_t>((len + BN - 1) / BN);
       if (n == 0) continue;
       const int64_t bh = u / G, g = u % G;
-      const uint16_t* kh = a.k + bh * a.Nk * D + chunk * 8;
-      const uint16_t* vh = a.v + bh * a.Nk * D + chunk * 8;
-      // index of row r of tile jj, -1 past the list, -2 when out of range
-      auto list_index = [&](uint32_t jj, int i) -> int {
-        const int r = row0 + i * C::kRowStep;
-        const int64_t pos = int64_t(jj) * BN + r;
-        if (r >= BN || pos >= len) return -1;
-        const int idx = __ldg(a.col_idx + begin + pos);
-        if (idx < 0 || idx >= a.Nk) {
-          bad_index = true;
-          return -2;
+      const uint16_t* kh = a.k + bh * a.Nk * D + sub * 8;
+      const uint16_t* vh = a.v + bh * a.Nk * D + sub * 8;
+      auto load_indices = [&](uint32_t jj, int* dst) {
+#pragma unroll
+        for (int i = 0; i < C::kKVRowsPerThread; ++i) {
+          const int r = row0 + i * C::kRowStep;
+          const int64_t pos = int64_t(jj) * BN + r;
+          if (r < BN && pos < len) dst[i] = __ldg(a.col_idx + begin + pos);
         }
-        return idx;
       };
+      // Issue one tile's copies: rows past the list, and flagged indices
+      // outside [0, Nk), are zero-filled.
+      auto issue = [&](uint32_t jj, const int* idx, uint32_t dst_base, const uint16_t* src_head,
+                       const uint16_t* any) {
 #pragma unroll
-      for (int i = 0; i < C::kKVRowsPerThread; ++i) idx_cur[i] = list_index(0, i);
-      // Q rows of the group (zero past the group / past Nq).
-      if (un > 0 && !mbar_wait(&bars->qempty, (un - 1) & 1, abort)) goto done;
+        for (int i = 0; i < C::kKVRowsPerThread; ++i) {
+          const int r = row0 + i * C::kRowStep;
+          if (r >= BN) break;
+          const int64_t pos = int64_t(jj) * BN + r;
+          const bool in_list = pos < len;
+          const bool ok = in_list && static_cast<uint32_t>(idx[i]) < static_cast<uint32_t>(a.Nk);
+          bad_index |= in_list && !ok;
+          const uint16_t* src = ok ? src_head + int64_t(idx[i]) * D : any;
 #pragma unroll
-      for (int i = 0; i < C::kQRowsPerThread; ++i) {
-        const int r = row0 + i * C::kRowStep;
-        if (r >= 128 * RB) break;
-        const int64_t grow = g * a.M + r;
-        const bool in = r < a.M && grow < a.Nq;
-        const uint16_t* src = in ? a.q + (bh * a.Nq + grow) * D + chunk * 8 : a.q;
-        cp_async16(q_addr + (r >> 7) * C::kQBlock + sw128_offset(r & 127, chunk, 128), src, in ? 16u : 0u);
+          for (int c = 0; c < C::kChunksPerLane; ++c)
+            cp_async16(dst_base + sw128_offset(r, sub + 8 * c, BN), src + 64 * c, ok ? 16u : 0u);
+        }
+      };
+      load_indices(0, idx_cur);
+      if (pt == 0) {
+        // query rows g*M .. g*M + 128*RB - 1 of this head (rows past the
+        // group feed only rows that are never written; past the tensor: zeros)
+        if (un > 0 && !mbar_wait(&bars->qempty, (un - 1) & 1, abort)) goto done;
+        mbar_expect_tx(&bars->qfull, C::kQBytes);
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+          for (int cb = 0; cb < D / 64; ++cb)
+            tma_load_2d(q_addr + rb * C::kQBlock + cb * 128 * 128, &tmq, 64 * cb,
+                        static_cast<int>(bh * a.Nq + g * a.M + rb * 128), &bars->qfull);
       }
-      cp_async_arrive_noinc(&bars->qfull);
       for (uint32_t j = 0; j <= n; ++j) {
         const uint32_t tt = t + j;
         if (j < n) {
-          if (j + 1 < n) {
-#pragma unroll
-            for (int i = 0; i < C::kKVRowsPerThread; ++i) idx_nxt[i] = list_index(j + 1, i);
-          }
+          if (j + 1 < n) load_indices(j + 1, idx_nxt);
           const uint32_t s = tt % STAGES;
           if (!mbar_wait(&bars->kempty[s], ((tt / STAGES) & 1) ^ 1, abort)) goto done;
-#pragma unroll
-          for (int i = 0; i < C::kKVRowsPerThread; ++i) {
-            const int r = row0 + i * C::kRowStep;
-            if (r >= BN) break;
-            const int idx = idx_cur[i];
-            const uint16_t* src = idx >= 0 ? kh + int64_t(idx) * D : a.k;
-            cp_async16(k_addr + s * C::kTile + sw128_offset(r, chunk, BN), src, idx >= 0 ? 16u : 0u);
-          }
+          issue(j, idx_cur, k_addr + s * C::kTile, kh, a.k);
           cp_async_arrive_noinc(&bars->kfull[s]);
         }
         if (j >= 1) {
           const uint32_t tp = tt - 1, s = tp % STAGES;
           if (!mbar_wait(&bars->vempty[s], ((tp / STAGES) & 1) ^ 1, abort)) goto done;
-#pragma unroll
-          for (int i = 0; i < C::kKVRowsPerThread; ++i) {
-            const int r = row0 + i * C::kRowStep;
-            if (r >= BN) break;
-            const int idx = idx_prv[i];
-            const uint16_t* src = idx >= 0 ? vh + int64_t(idx) * D : a.v;
-            cp_async16(v_addr + s * C::kTile + sw128_offset(r, chunk, BN), src, idx >= 0 ? 16u : 0u);
-          }
+          issue(j - 1, idx_prv, v_addr + s * C::kTile, vh, a.v);
           cp_async_arrive_noinc(&bars->vfull[s]);
         }
 #pragma unroll
@@ -472,7 +475,8 @@ done:
 }
 
 template <int D, int RB, int BN, int STAGES>
-static cudaError_t launch(const FwdArgs& a, int num_sms, cudaStream_t stream) {
+static cudaError_t launch(const FwdArgs& a, const CUtensorMap& tmq, int num_sms,
+                          cudaStream_t stream) {
   using C = FwdCfg<D, RB, BN, STAGES>;
   auto kern = sa_forward_kernel<D, RB, BN, STAGES>;
   // At least half the SM's shared memory, so that one CTA owns each SM's TMEM.
@@ -480,18 +484,21 @@ static cudaError_t launch(const FwdArgs& a, int num_sms, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t grid = a.units < num_sms ? a.units : num_sms;
-  kern<<<static_cast<unsigned>(grid), C::kThreads, smem, stream>>>(a);
+  kern<<<static_cast<unsigned>(grid), C::kThreads, smem, stream>>>(a, tmq);
   return cudaGetLastError();
 }
 
 cudaError_t launch_forward(const FwdArgs& a, int d, int num_sms, cudaStream_t stream) {
   if (a.units <= 0) return cudaSuccess;
+  const int64_t bh = a.units / a.G;
+  CUtensorMap tmq;
+  if (!make_rows_map(&tmq, a.q, uint64_t(bh) * a.Nq, d, 128)) return cudaErrorInvalidValue;
   if (d == 128) {
-    return a.M <= 128 ? launch<128, 1, 128, 3>(a, num_sms, stream)
-                      : launch<128, 2, 64, 4>(a, num_sms, stream);
+    return a.M <= 128 ? launch<128, 1, 128, 3>(a, tmq, num_sms, stream)
+                      : launch<128, 2, 64, 4>(a, tmq, num_sms, stream);
   }
-  return a.M <= 128 ? launch<64, 1, 128, 4>(a, num_sms, stream)
-                    : launch<64, 2, 64, 4>(a, num_sms, stream);
+  return a.M <= 128 ? launch<64, 1, 128, 4>(a, tmq, num_sms, stream)
+                    : launch<64, 2, 64, 4>(a, tmq, num_sms, stream);
 }
 
 }  // namespace sa
