@@ -44,6 +44,12 @@ CASES = [
     (128, 128, (4, 16, 16), None, "mass", {"mass": 0.5}),
     (64, 192, (5, 10, 20), (7, 10, 10), "mass", {"mass": 0.9}),
     (128, 128, (4, 16, 16), None, "mass", {"mass": 1.0}),
+    # more keys than the selection's in-memory bracket: the sampled path
+    (128, 128, (4, 16, 16), (10, 25, 40), "topk", {"topk": 2000}),
+    (128, 128, (4, 16, 16), (10, 25, 40), "topk", {"topk": 9}),
+    (128, 128, (4, 16, 16), (10, 25, 40), "topk", {"topk": 9990}),
+    (128, 128, (4, 16, 16), (10, 25, 40), "mass", {"mass": 0.99}),
+    (128, 128, (4, 16, 16), (10, 25, 40), "mass", {"mass": 0.3}),
 ]
 
 

@@ -311,87 +311,451 @@ struct SelArgs {
   uint32_t* cut;
   int32_t* ties;
   int64_t* counts;
+  int32_t* col_idx;      // TOPK only: lists are emitted by the select kernel
+  int64_t col_capacity;
 };
 
-constexpr int kSelThreads = 1024;
-constexpr int kBins = 2048;                 // radix levels of 11, 11 and 10 bits
+constexpr int kSelThreads = 256;            // one row per block, 4 blocks resident per SM
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kBins = 1024;                 // linear bins over the undecided score range
+constexpr int kBinsPerThread = kBins / kSelThreads;
+constexpr int kLevels = 3;                  // bin refinements of the crossing bin
+constexpr int kRank = 512;                  // exact ranking once this few keys are undecided
+constexpr int kWindow = 4096;               // keys the sampled bracket may hold
+constexpr int kSampleMax = 2 * kWindow;     // samples share the bracket's storage
+constexpr int kUnroll = 4;                  // float4 loads in flight per lane
+constexpr int kWinUnroll = 4;               // ... in the bracket pass (16 keys per lane)
 constexpr float kMassOne = 4294967296.0f;   // fixed-point unit of probability mass (2^32)
 
 // Probability mass exp(x - max) of one key in 2^-32 units; integer sums are
-// exact and order-independent, so every thread agrees on the crossing bin.
+// exact and order-independent, so every pass agrees on every partial sum.
 __device__ __forceinline__ unsigned long long fixed_mass(float x, float rmax) {
   return __float2ull_rn(expf(x - rmax) * kMassOne);
 }
 
+// One refinement level: keys in the undecided range are spread over kBins
+// linear bins starting at lo; `pick` is the bin that holds the cut.
+struct SelLevel {
+  float lo, inv;
+  int pick;
+};
+
+__device__ __forceinline__ int lin_bin(float x, float lo, float inv, int nb) {
+  const float f = (x - lo) * inv;
+  return f <= 0.f ? 0 : (f >= float(nb - 1) ? nb - 1 : static_cast<int>(f));
+}
+
+struct SelSmem {
+  uint32_t hist[kBins];
+  unsigned long long hmass[kBins];
+  float rx[kRank];
+  int32_t rj[kRank];
+  union {
+    struct {
+      float x[kWindow];
+      int32_t j[kWindow];
+    } win;
+    float sample[kSampleMax];
+  } u;
+  SelLevel levels[kLevels];
+  float fred[3][32];
+  int64_t scan_c[32], scan_m[32];
+  int32_t claim, n_rank, n_win, found_cnt, cut_rank;
+  int64_t found_above_cnt, found_above_mass, cut_greater;
+  float cut_x;
+  int32_t seg_sel[kSelWarps], seg_tie[kSelWarps];
+};
+
+// Keys of one row: either the whole score row or the bracketed window.
+struct RowSrc {
+  const float* s;
+  int n;
+  __device__ __forceinline__ float x(int i) const { return s[i]; }
+  __device__ __forceinline__ int j(int i) const { return i; }
+};
+struct WinSrc {
+  const float* xs;
+  const int32_t* js;
+  int n;
+  __device__ __forceinline__ float x(int i) const { return xs[i]; }
+  __device__ __forceinline__ int j(int i) const { return js[i]; }
+};
+
+__device__ __forceinline__ float block_min(float v, SelSmem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if (lane == 0) sm.fred[0][warp] = v;
+  __syncthreads();
+  v = sm.fred[0][0];
+#pragma unroll
+  for (int w = 1; w < kSelWarps; ++w) v = fminf(v, sm.fred[0][w]);
+  return v;
+}
+__device__ __forceinline__ float block_max(float v, SelSmem& sm) { return -block_min(-v, sm); }
+
+__device__ __forceinline__ float f4_get(const float4& v, int e) {
+  return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
+}
+
+// Calls f(j, x) for every key of a row; lanes read float4s, kUnroll of them
+// in flight, and the tail that does not fill a float4 is read singly.
+template <class F>
+__device__ __forceinline__ void for_each_key(const float* s, int Nk, F&& f) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nv = Nk >> 2;
+  const float4* s4 = reinterpret_cast<const float4*>(s);
+  for (int b = warp * 32 * kUnroll; b < nv; b += kSelThreads * kUnroll) {
+    float4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i4 = b + u * 32 + lane;
+      v[u] = i4 < nv ? __ldg(s4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i4 = b + u * 32 + lane;
+      if (i4 < nv) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f(4 * i4 + e, f4_get(v[u], e));
+      }
+    }
+  }
+  for (int j = 4 * nv + threadIdx.x; j < Nk; j += kSelThreads) f(j, s[j]);
+}
+
+// The exact selection among the undecided keys of `src` (all with scores in
+// [lo0, hi0]); `above_cnt` / `above_mass` account for the keys above hi0.
+// Keys are ranked by (score descending, index ascending).  TOPK takes rank
+// k-1 as the cut; MASS the first key at which the running fixed-point mass
+// reaches `target`.  Returns the cut as (order key, kept ties, row count).
+template <class Src>
+__device__ void exact_select(const Src& src, float lo0, float hi0, int64_t k, double target,
+                             bool by_mass, float rmax, int64_t above_cnt, int64_t above_mass,
+                             int64_t keep_all_count, SelSmem& sm, uint32_t* cut, int32_t* ties,
+                             int64_t* count) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int nlev = 0;
+  bool ranked = false, all_equal = false;
+  float lo = lo0, hi = hi0;
+  for (int lv = 0; lv < kLevels; ++lv) {
+    if (!(hi > lo)) {  // every undecided key has the same score
+      all_equal = true;
+      break;
+    }
+    const float inv = float(kBins) / (hi - lo);
+    for (int i = tid; i < kBins; i += kSelThreads) {
+      sm.hist[i] = 0;
+      if (by_mass) sm.hmass[i] = 0ull;
+    }
+    if (tid == 0) {
+      sm.levels[lv].lo = lo;
+      sm.levels[lv].inv = inv;
+      sm.levels[lv].pick = -1;
+      sm.claim = -1;
+    }
+    __syncthreads();
+    SelLevel lvl[kLevels];
+#pragma unroll
+    for (int i = 0; i < kLevels; ++i) lvl[i] = sm.levels[i];
+    for (int base = warp * 32; base < src.n; base += kSelThreads) {
+      const int i = base + lane;
+      const float x = i < src.n ? src.x(i) : -INFINITY;
+      bool in = i < src.n && x >= lo0 && x <= hi0;
+#pragma unroll
+      for (int l = 0; l < kLevels; ++l)
+        if (l < lv) in = in && lin_bin(x, lvl[l].lo, lvl[l].inv, kBins) == lvl[l].pick;
+      const int b = in ? lin_bin(x, lo, inv, kBins) : -1;
+      const unsigned same = __match_any_sync(0xffffffffu, b);
+      if (in && lane == __ffs(same) - 1) atomicAdd(&sm.hist[b], static_cast<uint32_t>(__popc(same)));
+      if (in && by_mass) atomicAdd(&sm.hmass[b], fixed_mass(x, rmax));
+    }
+    __syncthreads();
+    const int top = kBins - 1 - kBinsPerThread * tid;
+    int64_t c2 = 0, m2 = 0;
+#pragma unroll
+    for (int e = 0; e < kBinsPerThread; ++e) {
+      c2 += sm.hist[top - e];
+      if (by_mass) m2 += int64_t(sm.hmass[top - e]);
+    }
+    int64_t ctot, mtot = 0;
+    const int64_t cex = block_excl_scan<int64_t>(c2, &ctot, sm.scan_c);
+    const int64_t mex = by_mass ? block_excl_scan<int64_t>(m2, &mtot, sm.scan_m) : 0;
+    int64_t cum_c = above_cnt + cex, cum_m = above_mass + mex;
+    for (int e = 0; e < kBinsPerThread; ++e) {
+      const int bin = top - e;
+      const int64_t bc = sm.hist[bin], bm = by_mass ? int64_t(sm.hmass[bin]) : 0;
+      const bool cross = by_mass ? (bm > 0 && double(cum_m + bm) >= target && double(cum_m) < target)
+                                 : (bc > 0 && double(cum_c + bc) >= target && double(cum_c) < target);
+      if (cross && atomicCAS(&sm.claim, -1, bin) == -1) {
+        sm.found_cnt = static_cast<int32_t>(bc);
+        sm.found_above_cnt = cum_c - above_cnt;
+        sm.found_above_mass = cum_m - above_mass;
+      }
+      cum_c += bc;
+      cum_m += bm;
+    }
+    __syncthreads();
+    const int bin = sm.claim;
+    if (bin < 0) break;  // mass target beyond the rounded total
+    if (tid == 0) sm.levels[lv].pick = bin;
+    above_cnt += sm.found_above_cnt;
+    above_mass += sm.found_above_mass;
+    nlev = lv + 1;
+    const int bc = sm.found_cnt;
+    lo = lvl[lv].lo + float(bin) / inv;  // the picked bin's interval is the next range
+    hi = lvl[lv].lo + float(bin + 1) / inv;
+    __syncthreads();
+    if (bc <= kRank) {
+      ranked = true;
+      break;
+    }
+  }
+  __syncthreads();
+  if (nlev == 0 && !all_equal) {
+    *cut = 0;  // keep every key
+    *ties = 0;
+    *count = keep_all_count;
+    return;
+  }
+  SelLevel lvl[kLevels];
+#pragma unroll
+  for (int i = 0; i < kLevels; ++i) lvl[i] = sm.levels[i];
+  if (tid == 0) {
+    sm.n_rank = 0;
+    sm.cut_rank = -1;
+  }
+  __syncthreads();
+  for (int base = warp * 32; base < src.n; base += kSelThreads) {
+    const int i = base + lane;
+    const float x = i < src.n ? src.x(i) : -INFINITY;
+    bool in = i < src.n && x >= lo0 && x <= hi0;
+#pragma unroll
+    for (int l = 0; l < kLevels; ++l)
+      if (l < nlev) in = in && lin_bin(x, lvl[l].lo, lvl[l].inv, kBins) == lvl[l].pick;
+    const unsigned ballot = __ballot_sync(0xffffffffu, in);
+    int slot0 = 0;
+    if (lane == 0 && ballot) slot0 = atomicAdd(&sm.n_rank, __popc(ballot));
+    slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+    const int slot = slot0 + __popc(ballot & ((1u << lane) - 1u));
+    if (in && slot < kRank) {
+      sm.rx[slot] = x;
+      sm.rj[slot] = src.j(i);
+    }
+  }
+  __syncthreads();
+  const int n_und = sm.n_rank;
+  const int nc = n_und < kRank ? n_und : kRank;
+  if (!ranked || n_und > kRank) {
+    // The undecided keys share one score (the bin is below float
+    // resolution): the cut is that score and the tie rule decides.
+    const float xv = sm.rx[0];
+    *cut = order_key(xv);
+    int32_t t;
+    if (by_mass) {
+      const double e = static_cast<double>(fixed_mass(xv, rmax));
+      const double need = e > 0.0 ? ceil((target - double(above_mass)) / e) : 1.0;
+      t = static_cast<int32_t>(need < 1.0 ? 1 : (need > double(n_und) ? n_und : need));
+    } else {
+      t = static_cast<int32_t>(min64(k - above_cnt, n_und));
+    }
+    *ties = t;
+    *count = above_cnt + t;
+    return;
+  }
+  for (int c = tid; c < nc; c += kSelThreads) {
+    const float xc = sm.rx[c];
+    const int jc = sm.rj[c];
+    int rank = 0, greater = 0;
+    int64_t before_m = 0;
+    for (int o = 0; o < nc; ++o) {
+      const float xo = sm.rx[o];
+      const bool ahead = xo > xc || (xo == xc && sm.rj[o] < jc);
+      rank += ahead;
+      greater += xo > xc;
+      if (by_mass && ahead) before_m += int64_t(fixed_mass(xo, rmax));
+    }
+    bool is_cut;
+    if (by_mass) {
+      const int64_t incl = above_mass + before_m + int64_t(fixed_mass(xc, rmax));
+      is_cut = double(incl) >= target && double(above_mass + before_m) < target;
+    } else {
+      is_cut = above_cnt + rank == k - 1;
+    }
+    if (is_cut) {
+      sm.cut_rank = rank;
+      sm.cut_x = xc;
+      sm.cut_greater = greater;
+    }
+  }
+  __syncthreads();
+  if (sm.cut_rank < 0) {  // rounding left the mass target unreached
+    *cut = 0;
+    *ties = 0;
+    *count = keep_all_count;
+  } else {
+    *cut = order_key(sm.cut_x);
+    *count = above_cnt + sm.cut_rank + 1;
+    *ties = static_cast<int32_t>(*count - (above_cnt + sm.cut_greater));
+  }
+}
+
+// Writes the ascending indices of a row's kept keys (score above the cut, or
+// equal to it among the first `ties` such keys) to col_idx[base, end).  Each
+// warp owns one contiguous segment of the row: it counts its kept keys, the
+// segments' offsets come from one block-wide exchange, and a second read of
+// the segment writes the indices in order.
+__device__ void emit_row(const float* s, int Nk, uint32_t ck, int64_t nt, int64_t base, int64_t end,
+                         int32_t* col_idx, int32_t* seg_sel, int32_t* seg_tie) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nv = (Nk + 3) >> 2;  // float4 chunks, the last one possibly partial
+  const int per = (nv + kSelWarps - 1) / kSelWarps;
+  const int v0 = warp * per, v1 = min(v0 + per, nv);
+  const float4* s4 = reinterpret_cast<const float4*>(s);
+  auto load4 = [&](int i4, float* x) {
+    if (4 * i4 + 3 < Nk) {
+      const float4 v = __ldg(s4 + i4);
+      x[0] = v.x;
+      x[1] = v.y;
+      x[2] = v.z;
+      x[3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = 4 * i4 + e < Nk ? s[4 * i4 + e] : -INFINITY;
+    }
+  };
+  int n_sel = 0, n_tie = 0;
+  for (int b = v0; b < v1; b += 32 * kUnroll) {
+    float x[kUnroll][4];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i4 = b + u * 32 + lane;
+      if (i4 < v1) load4(i4, x[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i4 = b + u * 32 + lane;
+      if (i4 < v1) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool in = 4 * i4 + e < Nk;
+          const uint32_t kx = order_key(x[u][e]);
+          n_sel += in && kx > ck;
+          n_tie += in && kx == ck;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    n_sel += __shfl_xor_sync(0xffffffffu, n_sel, o);
+    n_tie += __shfl_xor_sync(0xffffffffu, n_tie, o);
+  }
+  __syncthreads();
+  if (lane == 0) {
+    seg_sel[warp] = n_sel;
+    seg_tie[warp] = n_tie;
+  }
+  __syncthreads();
+  int64_t sb = 0, tb = 0;
+  for (int w = 0; w < warp; ++w) {
+    sb += seg_sel[w];
+    tb += seg_tie[w];
+  }
+  for (int b0 = v0; b0 < v1; b0 += 32 * kUnroll) {
+    float xs[kUnroll][4];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i4 = b0 + u * 32 + lane;
+      if (i4 < v1) load4(i4, xs[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+    const int b = b0 + u * 32;
+    if (b >= v1) break;
+    const int i4 = b + lane;
+    float* x = xs[u];
+    bool sel[4], tie[4];
+    int cs = 0, ct = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const bool in = i4 < v1 && 4 * i4 + e < Nk;
+      const uint32_t kx = in ? order_key(x[e]) : 0u;
+      sel[e] = in && kx > ck;
+      tie[e] = in && kx == ck;
+      cs += sel[e];
+      ct += tie[e];
+    }
+    // exclusive prefix of (sel, tie) counts over the warp's lanes
+    int ps = cs, pt = ct;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a1 = __shfl_up_sync(0xffffffffu, ps, o), a2 = __shfl_up_sync(0xffffffffu, pt, o);
+      if (lane >= o) {
+        ps += a1;
+        pt += a2;
+      }
+    }
+    const int tot_s = __shfl_sync(0xffffffffu, ps, 31), tot_t = __shfl_sync(0xffffffffu, pt, 31);
+    int64_t ls = sb + ps - cs, lt = tb + pt - ct;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (sel[e]) {
+        const int64_t pos = base + ls + min64(lt, nt);
+        if (pos < end) col_idx[pos] = 4 * i4 + e;
+        ++ls;
+      } else if (tie[e]) {
+        const int64_t pos = base + ls + lt;
+        if (lt < nt && pos < end) col_idx[pos] = 4 * i4 + e;
+        ++lt;
+      }
+    }
+    sb += tot_s;
+    tb += tot_t;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kSelThreads) sa_select_kernel(const SelArgs a) {
-  __shared__ uint32_t hist[kBins];
-  __shared__ unsigned long long hmass[kBins];
-  __shared__ float red_m[32], red_z[32];
-  __shared__ int64_t scan_c[32], scan_m[32];
-  __shared__ int32_t claim;
-  __shared__ int32_t found_cnt;
-  __shared__ int64_t found_above_cnt, found_above_mass;
+  extern __shared__ uint8_t sel_raw[];
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(sel_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.x;
   const float* s = a.scores + row * a.ld;
   const int Nk = a.Nk;
-
-  float rmax = -INFINITY, rz = 0.f;
-  if (a.mode != SA_SELECT_TOPK) {
-    // row max and sum of exp(x - max), one pass with rescaling
-    float m = -INFINITY, z = 0.f;
-    for (int j = tid; j < Nk; j += kSelThreads) {
-      const float x = s[j];
-      if (x > m) {
-        z = z * expf(m - x) + 1.f;
-        m = x;
-      } else {
-        z += expf(x - m);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), z2 = __shfl_xor_sync(0xffffffffu, z, o);
-      const float mm = fmaxf(m, m2);
-      z = (m == -INFINITY ? 0.f : z * expf(m - mm)) + (m2 == -INFINITY ? 0.f : z2 * expf(m2 - mm));
-      m = mm;
-    }
-    if (lane == 0) {
-      red_m[warp] = m;
-      red_z[warp] = z;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      m = red_m[lane];
-      z = red_z[lane];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o), z2 = __shfl_xor_sync(0xffffffffu, z, o);
-        const float mm = fmaxf(m, m2);
-        z = (m == -INFINITY ? 0.f : z * expf(m - mm)) + (m2 == -INFINITY ? 0.f : z2 * expf(m2 - mm));
-        m = mm;
-      }
-      if (lane == 0) {
-        red_m[0] = m;
-        red_z[0] = z;
-      }
-    }
-    __syncthreads();
-    rmax = red_m[0];
-    rz = red_z[0];
-  }
-
+  const bool by_mass = a.mode == SA_SELECT_MASS;
   uint32_t cut = 0;
   int32_t ties = 0;
   int64_t count = Nk;
+
   if (a.mode == SA_SELECT_THRESHOLD) {
     // keep p_j >= tau  <=>  sigma_j >= ln tau + max + ln Z
+    float mx = -INFINITY, z = 0.f;
+    for_each_key(s, Nk, [&](int, float x) {
+      if (x > mx) {
+        z = z * expf(mx - x) + 1.f;
+        mx = x;
+      } else {
+        z += expf(x - mx);
+      }
+    });
+    const float rmax = block_max(mx, sm);
+    float zr = (mx == -INFINITY) ? 0.f : z * expf(mx - rmax);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) zr += __shfl_xor_sync(0xffffffffu, zr, o);
+    __syncthreads();
+    if (lane == 0) sm.fred[1][warp] = zr;
+    __syncthreads();
+    float rz = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSelWarps; ++w) rz += sm.fred[1][w];
     const float c = a.log_tau + rmax + logf(rz);
     const uint32_t kc = (c == -INFINITY) ? 0u : order_key(c);
     int64_t n = 0;
-    for (int j = tid; j < Nk; j += kSelThreads) n += order_key(s[j]) >= kc;
+    for_each_key(s, Nk, [&](int, float x) { n += order_key(x) >= kc; });
     int64_t total;
-    block_excl_scan<int64_t>(n, &total, scan_c);
+    block_excl_scan<int64_t>(n, &total, sm.scan_c);
     if (total > 0) {
       cut = kc > 0 ? kc - 1 : 0u;  // keys > kc - 1  <=>  keys >= kc
       ties = 0;
@@ -401,94 +765,214 @@ __global__ void __launch_bounds__(kSelThreads) sa_select_kernel(const SelArgs a)
       ties = 1;
       count = 1;
     }
-  } else if (a.mode == SA_SELECT_MASS && a.mass >= 1.0) {
+  } else if (by_mass && a.mass >= 1.0) {
     cut = 0;  // the whole mass needs every key
     ties = 0;
     count = Nk;
   } else {
-    const bool by_mass = a.mode == SA_SELECT_MASS;
     const int64_t k = min64(max64(a.topk, 1), Nk);
+    float rmax = 0.f;
     double target = static_cast<double>(k);
-    uint32_t prefix = 0, pmask = 0;
-    int64_t above_cnt = 0, above_mass = 0;
-    int32_t last_cnt = 0;
-    bool keep_all = false;
-    const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
-    for (int lv = 0; lv < 3; ++lv) {
-      const int shift = shifts[lv], nb = 1 << widths[lv];
-      for (int i = tid; i < kBins; i += kSelThreads) {
-        hist[i] = 0;
-        hmass[i] = 0ull;
-      }
-      if (tid == 0) claim = -1;
-      __syncthreads();
-      for (int j = tid; j < Nk; j += kSelThreads) {
-        const float x = s[j];
-        const uint32_t kx = order_key(x);
-        if ((kx & pmask) == prefix) {
-          const uint32_t bin = (kx >> shift) & (nb - 1);
-          atomicAdd(&hist[bin], 1u);
-          if (by_mass) atomicAdd(&hmass[bin], fixed_mass(x, rmax));
-        }
-      }
-      __syncthreads();
-      // Thread t owns bins nb-1-2t and nb-2-2t (descending score order).
-      const int top = nb - 1 - 2 * tid;
-      int64_t c2 = 0, m2 = 0;
-      if (top >= 0) {
-        c2 = int64_t(hist[top]) + hist[top - 1];
-        m2 = int64_t(hmass[top]) + int64_t(hmass[top - 1]);
-      }
-      int64_t ctot, mtot;
-      const int64_t cex = block_excl_scan<int64_t>(c2, &ctot, scan_c);
-      const int64_t mex = block_excl_scan<int64_t>(m2, &mtot, scan_m);
-      if (by_mass && lv == 0) target = a.mass * static_cast<double>(mtot);
-      if (top >= 0) {
-        int64_t cum_c = above_cnt + cex, cum_m = above_mass + mex;
-        for (int e = 0; e < 2; ++e) {
-          const int bin = top - e;
-          const int64_t bc = hist[bin], bm = int64_t(hmass[bin]);
-          const bool cross = by_mass
-                                 ? (bm > 0 && double(cum_m + bm) >= target && double(cum_m) < target)
-                                 : (bc > 0 && double(cum_c + bc) >= target && double(cum_c) < target);
-          if (cross && atomicCAS(&claim, -1, bin) == -1) {
-            found_cnt = static_cast<int32_t>(bc);
-            found_above_cnt = cum_c - above_cnt;
-            found_above_mass = cum_m - above_mass;
-          }
-          cum_c += bc;
-          cum_m += bm;
-        }
-      }
-      __syncthreads();
-      const int bin = claim;
-      if (bin < 0) {
-        keep_all = true;  // target not reachable through rounding: keep every key
-        break;
-      }
-      prefix |= static_cast<uint32_t>(bin) << shift;
-      pmask |= static_cast<uint32_t>(nb - 1) << shift;
-      above_cnt += found_above_cnt;
-      above_mass += found_above_mass;
-      last_cnt = found_cnt;
-      __syncthreads();
+    if (by_mass) {
+      float mx = -INFINITY;
+      for_each_key(s, Nk, [&](int, float x) { mx = fmaxf(mx, x); });
+      rmax = block_max(mx, sm);
+      unsigned long long zt = 0;
+      for_each_key(s, Nk, [&](int, float x) { zt += fixed_mass(x, rmax); });
+      int64_t ztot;
+      block_excl_scan<int64_t>(static_cast<int64_t>(zt), &ztot, sm.scan_m);
+      target = a.mass * static_cast<double>(ztot);
     }
-    if (keep_all) {
-      cut = 0;
-      ties = 0;
-      count = Nk;
-    } else if (by_mass) {
-      // every key equal to the cut carries the same fixed-point mass
-      const double e = static_cast<double>(fixed_mass(key_value(prefix), rmax));
-      const double need = e > 0.0 ? ceil((target - double(above_mass)) / e) : 1.0;
-      const int32_t n = need < 1.0 ? 1 : (need > double(last_cnt) ? last_cnt : static_cast<int32_t>(need));
-      cut = prefix;
-      ties = n;
-      count = above_cnt + n;
+    // ---- bracket the cut from an evenly strided sample of the row
+    float lo = -INFINITY, hi = INFINITY;
+    if (Nk > kWindow) {
+      const int S = Nk / 4 < kSampleMax ? (Nk / 4 > 1024 ? Nk / 4 : 1024) : kSampleMax;
+      const int stride = Nk / S;  // >= 1: samples j = i*stride, evenly spread over the row
+      float smn = INFINITY, smx = -INFINITY;
+#pragma unroll 8
+      for (int i = tid; i < S; i += kSelThreads) {
+        const float x = __ldg(s + i * stride);
+        sm.u.sample[i] = x;
+        smn = fminf(smn, x);
+        smx = fmaxf(smx, x);
+      }
+      smn = block_min(smn, sm);
+      smx = block_max(smx, sm);
+      if (smx > smn) {
+        const float inv = float(kBins) / (smx - smn);
+        for (int i = tid; i < kBins; i += kSelThreads) {
+          sm.hist[i] = 0;
+          if (by_mass) sm.hmass[i] = 0ull;
+        }
+        __syncthreads();
+        for (int i = tid; i < S; i += kSelThreads) {
+          const float x = sm.u.sample[i];
+          const int bn = lin_bin(x, smn, inv, kBins);
+          atomicAdd(&sm.hist[bn], 1u);
+          if (by_mass) atomicAdd(&sm.hmass[bn], fixed_mass(x, rmax));
+        }
+        __syncthreads();
+        const int top = kBins - 1 - kBinsPerThread * tid;
+        int64_t c4 = 0, m4 = 0;
+#pragma unroll
+        for (int e = 0; e < kBinsPerThread; ++e) {
+          c4 += sm.hist[top - e];
+          if (by_mass) m4 += int64_t(sm.hmass[top - e]);
+        }
+        int64_t ctot, mtot = 0;
+        const int64_t cex = block_excl_scan<int64_t>(c4, &ctot, sm.scan_c);
+        const int64_t mex = by_mass ? block_excl_scan<int64_t>(m4, &mtot, sm.scan_m) : 0;
+        // expected rank of the cut among the samples, counted from the top
+        double p;
+        if (by_mass) {
+          if (tid == 0) sm.found_above_cnt = S;  // no crossing: bracket everything below the top
+          __syncthreads();
+          const double share = a.mass * double(mtot);
+          int64_t cm = mex, cc = cex;
+          for (int e = 0; e < kBinsPerThread; ++e) {
+            const int64_t bm = int64_t(sm.hmass[top - e]), bc = sm.hist[top - e];
+            if (bm > 0 && double(cm + bm) >= share && double(cm) < share) sm.found_above_cnt = cc + bc;
+            cm += bm;
+            cc += bc;
+          }
+          __syncthreads();
+          p = double(sm.found_above_cnt);
+        } else {
+          p = double(k) * S / double(Nk);
+        }
+        const double q = fmin(fmax(p / S, 0.0), 1.0);
+        const double delta = 5.0 * sqrt(double(S) * q * (1.0 - q)) + 16.0;
+        const double r_hi = p - delta, r_lo = p + delta;  // sample ranks bounding the cut
+        if (tid == 0) {
+          sm.fred[2][0] = INFINITY;
+          sm.fred[2][1] = -INFINITY;
+        }
+        __syncthreads();
+        int64_t cc = cex;
+        for (int e = 0; e < kBinsPerThread; ++e) {
+          const int bn = top - e;
+          const int64_t bc = sm.hist[bn];
+          // this bin covers sample ranks [cc, cc + bc)
+          if (bc > 0 && r_hi >= double(cc) && r_hi < double(cc + bc)) sm.fred[2][0] = smn + float(bn + 1) / inv;
+          if (bc > 0 && r_lo >= double(cc) && r_lo < double(cc + bc)) sm.fred[2][1] = smn + float(bn) / inv;
+          cc += bc;
+        }
+        __syncthreads();
+        hi = r_hi >= 0.0 ? sm.fred[2][0] : INFINITY;
+        lo = r_lo < double(S) ? sm.fred[2][1] : -INFINITY;
+      } else {
+        lo = hi = smn;  // flat sample: try its single value, fall back if wrong
+      }
+      __syncthreads();  // the sample's storage becomes the bracket's
+    }
+    // ---- one pass: count the keys above the bracket, collect those inside
+    if (tid == 0) sm.n_win = 0;
+    __syncthreads();
+    int64_t c_above = 0;
+    unsigned long long m_above = 0, m_win = 0;
+    {
+      const int nv = Nk >> 2;
+      const float4* s4 = reinterpret_cast<const float4*>(s);
+      constexpr int U = kWinUnroll;
+      for (int b = warp * 32 * U; b < nv + 32 * U; b += kSelThreads * U) {
+        float x[U][4];
+        int jb[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i4 = b + u * 32 + lane;
+          jb[u] = 4 * i4;
+          if (i4 < nv) {
+            const float4 v = __ldg(s4 + i4);
+            x[u][0] = v.x;
+            x[u][1] = v.y;
+            x[u][2] = v.z;
+            x[u][3] = v.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[u][e] = 4 * i4 + e < Nk ? s[4 * i4 + e] : -INFINITY;
+          }
+        }
+        if (b >= nv && (4 * b >= Nk)) break;
+        int n_in = 0;
+        uint32_t in_mask = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float xv = x[u][e];
+            const bool valid = jb[u] + e < Nk;
+            const bool above = valid && xv > hi;
+            const bool inw = valid && xv >= lo && xv <= hi;
+            c_above += above;
+            if (by_mass && (above || inw)) {
+              const unsigned long long fm = fixed_mass(xv, rmax);
+              if (above) m_above += fm;
+              else m_win += fm;
+            }
+            in_mask |= (inw ? 1u : 0u) << (u * 4 + e);
+            n_in += inw;
+          }
+        // warp-aggregated append of this lane's in-bracket keys
+        int pre = n_in;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, pre, o);
+          if (lane >= o) pre += t;
+        }
+        const int tot = __shfl_sync(0xffffffffu, pre, 31);
+        int slot0 = 0;
+        if (lane == 0 && tot) slot0 = atomicAdd(&sm.n_win, tot);
+        int slot = __shfl_sync(0xffffffffu, slot0, 0) + pre - n_in;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (in_mask >> (u * 4 + e) & 1u) {
+              if (slot < kWindow) {
+                sm.u.win.x[slot] = x[u][e];
+                sm.u.win.j[slot] = jb[u] + e;
+              }
+              ++slot;
+            }
+      }
+    }
+    int64_t above_cnt, above_mass = 0, win_mass = 0;
+    block_excl_scan<int64_t>(c_above, &above_cnt, sm.scan_c);
+    if (by_mass) {
+      block_excl_scan<int64_t>(static_cast<int64_t>(m_above), &above_mass, sm.scan_m);
+      block_excl_scan<int64_t>(static_cast<int64_t>(m_win), &win_mass, sm.scan_c);
+    }
+    const int n_win = sm.n_win;
+    const bool bracketed =
+        n_win <= kWindow && (by_mass ? (double(above_mass) < target && target <= double(above_mass + win_mass))
+                                     : (above_cnt < k && k <= above_cnt + n_win));
+    if (bracketed) {
+      float wmn = INFINITY, wmx = -INFINITY;
+      for (int i = tid; i < n_win; i += kSelThreads) {
+        wmn = fminf(wmn, sm.u.win.x[i]);
+        wmx = fmaxf(wmx, sm.u.win.x[i]);
+      }
+      wmn = block_min(wmn, sm);
+      wmx = block_max(wmx, sm);
+      exact_select(WinSrc{sm.u.win.x, sm.u.win.j, n_win}, wmn, wmx, k, target, by_mass, rmax, above_cnt,
+                   above_mass, Nk, sm, &cut, &ties, &count);
     } else {
-      cut = prefix;
-      ties = static_cast<int32_t>(k - above_cnt);
-      count = k;
+      // The sample missed (or the bracket overflowed): select over the row.
+      float mn = INFINITY, mx = -INFINITY;
+      for_each_key(s, Nk, [&](int, float x) {
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
+      });
+      mn = block_min(mn, sm);
+      mx = block_max(mx, sm);
+      exact_select(RowSrc{s, Nk}, mn, mx, k, target, by_mass, rmax, 0, 0, Nk, sm, &cut, &ties, &count);
+    }
+    if (!by_mass && a.col_idx) {
+      // TOPK: every row holds exactly k keys, so row r starts at r*k and
+      // the lists are written here while the row is still in L2.
+      const int64_t base = row * k;
+      if (base + k <= a.col_capacity)
+        emit_row(s, Nk, cut, ties, base, base + k, a.col_idx, sm.seg_sel, sm.seg_tie);
     }
   }
   if (tid == 0) {
@@ -521,60 +1005,17 @@ __global__ void __launch_bounds__(1024) sa_scan_kernel(const int64_t* counts, in
 }
 
 // ------------------------------------------------------------ 5. emit
+// THRESHOLD and MASS: lists are written after row_ptr is known.
 __global__ void __launch_bounds__(kSelThreads) sa_emit_kernel(const float* scores, int64_t ld,
                                                               int32_t Nk, const uint32_t* cut,
                                                               const int32_t* ties,
                                                               const int64_t* row_ptr,
                                                               int32_t* col_idx, int64_t capacity) {
-  __shared__ int32_t scratch[32];
+  __shared__ int32_t seg_sel[kSelWarps], seg_tie[kSelWarps];
   const int64_t row = blockIdx.x;
   const int64_t base = row_ptr[row], end = row_ptr[row + 1];
   if (end > capacity) return;  // reported by the scan
-  const float* s = scores + row * ld;
-  const uint32_t ck = cut[row];
-  const int64_t nt = ties[row];
-  int64_t run_sel = 0, run_tie = 0;
-  for (int64_t c0 = 0; c0 < Nk; c0 += 4 * kSelThreads) {
-    const int64_t j0 = c0 + 4 * threadIdx.x;
-    float x[4];
-    if (j0 + 3 < Nk) {
-      const float4 v = *reinterpret_cast<const float4*>(s + j0);
-      x[0] = v.x;
-      x[1] = v.y;
-      x[2] = v.z;
-      x[3] = v.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) x[e] = j0 + e < Nk ? s[j0 + e] : -INFINITY;
-    }
-    bool sel[4], tie[4];
-    int32_t packed = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const bool in = j0 + e < Nk;
-      const uint32_t kx = order_key(x[e]);
-      sel[e] = in && kx > ck;
-      tie[e] = in && kx == ck;
-      packed += (sel[e] ? 1 : 0) + (tie[e] ? 0x10000 : 0);
-    }
-    int32_t total;
-    const int32_t ex = block_excl_scan<int32_t>(packed, &total, scratch);
-    int64_t sb = run_sel + (ex & 0xFFFF), tb = run_tie + (ex >> 16);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (sel[e]) {
-        const int64_t pos = base + sb + min64(tb, nt);
-        if (pos < end) col_idx[pos] = static_cast<int32_t>(j0 + e);
-        ++sb;
-      } else if (tie[e]) {
-        const int64_t pos = base + sb + tb;
-        if (tb < nt && pos < end) col_idx[pos] = static_cast<int32_t>(j0 + e);
-        ++tb;
-      }
-    }
-    run_sel += total & 0xFFFF;
-    run_tie += total >> 16;
-  }
+  emit_row(scores + row * ld, Nk, cut[row], ties[row], base, end, col_idx, seg_sel, seg_tie);
 }
 
 // ------------------------------------------------------------ validator
@@ -686,12 +1127,18 @@ cudaError_t launch_build_index(const BuildArgs& a, int num_sms, cudaStream_t st)
   s.cut = reinterpret_cast<uint32_t*>(a.ws + a.L.cut);
   s.ties = reinterpret_cast<int32_t*>(a.ws + a.L.ties);
   s.counts = reinterpret_cast<int64_t*>(a.ws + a.L.counts);
-  sa_select_kernel<<<static_cast<unsigned>(a.rows), kSelThreads, 0, st>>>(s);
+  s.col_idx = a.mode == SA_SELECT_TOPK ? a.col_idx : nullptr;
+  s.col_capacity = a.col_capacity;
+  e = cudaFuncSetAttribute(sa_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(sizeof(SelSmem)));
+  if (e != cudaSuccess) return e;
+  sa_select_kernel<<<static_cast<unsigned>(a.rows), kSelThreads, sizeof(SelSmem), st>>>(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   sa_scan_kernel<<<1, 1024, 0, st>>>(s.counts, a.rows, a.row_ptr, misc, a.col_capacity, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  sa_emit_kernel<<<static_cast<unsigned>(a.rows), kSelThreads, 0, st>>>(
-      s.scores, s.ld, a.Nk, s.cut, s.ties, a.row_ptr, a.col_idx, a.col_capacity);
+  if (a.mode != SA_SELECT_TOPK)
+    sa_emit_kernel<<<static_cast<unsigned>(a.rows), kSelThreads, 0, st>>>(
+        s.scores, s.ld, a.Nk, s.cut, s.ties, a.row_ptr, a.col_idx, a.col_capacity);
   return cudaGetLastError();
 }
 

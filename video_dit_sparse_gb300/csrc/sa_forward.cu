@@ -300,8 +300,17 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
       constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
       constexpr uint32_t kIdescSum = idesc_bf16(128, 16, false, false);
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      // Descriptor halves: the high words are constant, the low word holds the
+      // start address in 16-byte units (tiles lie below 256 KB of shared memory,
+      // so adding to it never carries into the leading-offset field).
+      const uint64_t dq = sw128_desc(q_addr, 16, 1024), dk = sw128_desc(k_addr, 16, 1024);
+      const uint64_t dv = sw128_desc(v_addr, BN * 128, 1024);
+      const uint32_t q_lo = static_cast<uint32_t>(dq), q_hi = static_cast<uint32_t>(dq >> 32);
+      const uint32_t k_lo = static_cast<uint32_t>(dk), k_hi = static_cast<uint32_t>(dk >> 32);
+      const uint32_t v_lo = static_cast<uint32_t>(dv), v_hi = static_cast<uint32_t>(dv >> 32);
       // 16 x 16 ones, no swizzle: 8x16-byte core matrices, 128 B / 256 B apart
       const uint64_t ones_desc = plain_desc(smem_u32(sOnes), 128, 256);
+      const uint32_t o_lo = static_cast<uint32_t>(ones_desc), o_hi = static_cast<uint32_t>(ones_desc >> 32);
       uint32_t t = 0, un = 0;
       bool ok = true;
       // O += P V for tile tt (first: overwrite O).
@@ -316,17 +325,17 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           tc_fence_after();
           const uint32_t a_tmem = tmem + b * C::kSCols + rb * BN;
           const uint32_t d_tmem = tmem + C::kOCol + rb * D;
+          const uint32_t vs_lo = v_lo + ((s * C::kTile) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t bdesc = sw128_desc(v_addr + s * C::kTile + kk * 2048, BN * 128, 1024);
-            mma_ts(d_tmem, a_tmem + kk * 8, bdesc, kIdescPV, (!first || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts_w(d_tmem, a_tmem + kk * 8, vs_lo + ((kk * 2048) >> 4), v_hi, kIdescPV,
+                     (!first || kk > 0) ? 1u : 0u);
           if (C::kSumMma) {
             // row sums of the bf16 P: P x ones, accumulated like O
             const uint32_t d_sum = tmem + C::kSumCol + rb * 16;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ts(d_sum, a_tmem + kk * 8, ones_desc, kIdescSum, (!first || kk > 0) ? 1u : 0u);
+              mma_ts_w(d_sum, a_tmem + kk * 8, o_lo, o_hi, kIdescSum, (!first || kk > 0) ? 1u : 0u);
           }
           mma_commit(&bars->pvdone[b][rb]);
         }
@@ -345,15 +354,15 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           if (!mbar_wait(&bars->kfull[s], (tt / STAGES) & 1, abort)) { ok = false; break; }
           fence_proxy_async_smem();  // K rows were written through the generic proxy
           tc_fence_after();
+          const uint32_t ks_lo = k_lo + ((s * C::kTile) >> 4);
 #pragma unroll
           for (int rb = 0; rb < RB; ++rb) {
             const uint32_t d_tmem = tmem + b * C::kSCols + rb * BN;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t adesc = sw128_desc(q_addr + rb * C::kQBlock + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024);
-              const uint64_t bdesc = sw128_desc(k_addr + s * C::kTile + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024);
-              mma_ss(d_tmem, adesc, bdesc, kIdescS, kk > 0 ? 1u : 0u);
-            }
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss_w(d_tmem, q_lo + ((rb * C::kQBlock + (kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4), q_hi,
+                       ks_lo + (((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4), k_hi, kIdescS,
+                       kk > 0 ? 1u : 0u);
             mma_commit(&bars->sfull[b][rb]);
           }
           mma_commit(&bars->kempty[s]);
