@@ -197,6 +197,18 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint3
       : "memory");
 }
 
+// Copies a 128-row x 32-byte slice of a shared-memory matrix (described by a
+// matrix descriptor, as for an MMA operand) into 128 TMEM lanes x 8 columns.
+// Ordered with the MMAs this thread issues later.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint32_t d_lo, uint32_t d_hi) {
+  asm volatile(
+      "{\n\t.reg .b64 d;\n\t"
+      "mov.b64 d, {%1, %2};\n\t"
+      "tcgen05.cp.cta_group::1.128x256b [%0], d;\n\t}" ::"r"(taddr),
+      "r"(d_lo), "r"(d_hi)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -302,6 +314,50 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c, int rows) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Pairs of fp32 values in one 64-bit register pair, for the packed
+// two-lane fp32 instructions.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2lo(uint64_t v) {
+  float r;
+  asm("{\n\t.reg .f32 t;\n\tmov.b64 {%0, t}, %1;\n\t}" : "=f"(r) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ float f2hi(uint64_t v) {
+  float r;
+  asm("{\n\t.reg .f32 t;\n\tmov.b64 {t, %0}, %1;\n\t}" : "=f"(r) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// acc + both bf16 halves of a packed pair (each widened exactly to fp32).
+__device__ __forceinline__ float add_bf16x2(uint32_t packed, float acc) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t.reg .f32 t;\n\t"
+      "mov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.bf16 t, lo, %2;\n\t"
+      "add.rn.f32.bf16 %0, hi, t;\n\t}"
+      : "=f"(r)
+      : "r"(packed), "f"(acc));
   return r;
 }
 

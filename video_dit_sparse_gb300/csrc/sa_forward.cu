@@ -51,15 +51,15 @@ struct FwdCfg {
   static constexpr int kTile = BN * D * 2;       // one K or V tile
   static constexpr int kSCols = RB * BN;         // TMEM columns per S buffer
   static constexpr int kOCol = 2 * kSCols;
-  // The bf16-rounded row sum comes from an extra MMA, P x ones (N = 16),
-  // when TMEM has room for its 16 columns per row block.
-  static constexpr bool kSumMma = 2 * kSCols + RB * (D + 16) <= 512;
-  static constexpr int kSumCol = kOCol + RB * D;
-  static constexpr int kUsedCols = 2 * kSCols + RB * D + (kSumMma ? 16 * RB : 0);
+  // Q moves from shared memory into TMEM (D/2 columns per 128-row block) once
+  // per unit, so the QK^T MMAs read only K from shared memory, when TMEM has
+  // room for it.
+  static constexpr int kQCol = kOCol + RB * D;
+  static constexpr bool kQTmem = kQCol + RB * D / 2 <= 512;
+  static constexpr int kUsedCols = kQCol + (kQTmem ? RB * D / 2 : 0);
   static constexpr int kTmemCols = kUsedCols <= 128 ? 128 : (kUsedCols <= 256 ? 256 : 512);
-  static constexpr int kOnesBytes = 1024;        // bf16 ones (512 B used) for the sum MMA
   static constexpr int kBarBytes = 1024;
-  static constexpr int kSmemBytes = 1024 + kQBytes + 2 * STAGES * kTile + kOnesBytes + kBarBytes;
+  static constexpr int kSmemBytes = 1024 + kQBytes + 2 * STAGES * kTile + kBarBytes;
   static_assert(kUsedCols <= 512, "TMEM budget");
   static_assert(BN % 64 == 0 && D % 64 == 0, "tile shapes");
   static_assert(kProdThreads % kLanesPerRow == 0 && kChunksPerLane >= 1, "gather mapping");
@@ -98,16 +98,10 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + C::kQBytes;
   uint8_t* sV = sK + STAGES * C::kTile;
-  uint8_t* sOnes = sV + STAGES * C::kTile;
-  Bars* bars = reinterpret_cast<Bars*>(sOnes + C::kOnesBytes);
+  Bars* bars = reinterpret_cast<Bars*>(sV + STAGES * C::kTile);
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (C::kSumMma && threadIdx.x < 32) {
-    // 512 bytes of bf16 1.0, read by the tensor core through the async proxy
-    reinterpret_cast<uint4*>(sOnes)[threadIdx.x] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-    fence_proxy_async_smem();
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars->kfull[s], C::kProdThreads);
@@ -186,16 +180,18 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           for (int c = 0; c < BN; ++c)
             if (c >= nvalid) x[c] = -INFINITY;
         }
-        // Row max of the raw scores (scale > 0 commutes with max), 8 chains.
+        // Row max of the raw scores (scale > 0 commutes with max): 3-input
+        // maxima in 8 chains.
         float mx;
         {
           float t8[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) t8[i] = x[i];
+          for (int i = 0; i < 8; ++i) t8[i] = fmaxf(x[i], x[8 + i]);
 #pragma unroll
-          for (int c = 8; c < BN; ++c) t8[c & 7] = fmaxf(t8[c & 7], x[c]);
-          mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
-                     fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+          for (int c = 16; c < BN; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t8[i] = fmax3(t8[i], x[c + i], x[c + 8 + i]);
+          mx = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
         }
         mx *= sl;
         if (j == 0) {
@@ -222,32 +218,29 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
             tmem_st32(obase + c * 32, r);
           }
-          if (C::kSumMma) {
-            const uint32_t saddr = tmem + lane_base + C::kSumCol + rb * 16;
-            const float sv = __uint_as_float(tmem_ld1(saddr)) * alpha;
-            tmem_st1(saddr, __float_as_uint(sv));
-          }
           tmem_st_wait();
         }
-        // P = exp2(s*x - m): one FFMA + EX2 per element.  The fp32 row sum
-        // (8 chains) feeds the log-sum-exp; O is normalised by the sum of
-        // the bf16-rounded P that the PV MMA consumes (an extra MMA against
-        // a ones tile, or here on the ALU when TMEM has no room for it).
-        const float nm = -m;
+        // P = exp2(s*x - m): a packed two-lane FFMA per pair, then EX2.  The
+        // fp32 sum of P gives the log-sum-exp; O is normalised by the sum of
+        // the bf16-rounded P that the PV MMA consumes, so that O stays a
+        // convex combination of V rows whatever the rounding.
+        const uint64_t sl2 = f2(sl, sl), nm2 = f2(-m, -m);
         uint32_t p[BN / 2];
-        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        float pr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        uint64_t ps[4] = {0, 0, 0, 0};
+        float pr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < BN / 2; ++c) {
-          const float p0 = fast_exp2(fmaf(x[2 * c], sl, nm));
-          const float p1 = fast_exp2(fmaf(x[2 * c + 1], sl, nm));
+          const uint64_t y = fma2(f2(x[2 * c], x[2 * c + 1]), sl2, nm2);
+          const float p0 = fast_exp2(f2lo(y)), p1 = fast_exp2(f2hi(y));
           p[c] = pack_bf16(p0, p1);
-          ps[c & 7] += p0 + p1;
-          if (!C::kSumMma)
-            pr[c & 7] += __uint_as_float(p[c] << 16) + __uint_as_float(p[c] & 0xFFFF0000u);
+          ps[c & 3] = add2(ps[c & 3], f2(p0, p1));
+          pr[c & 3] = add_bf16x2(p[c], pr[c & 3]);
         }
-        l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-        if (!C::kSumMma) lr += ((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7]));
+        {
+          const uint64_t s2 = add2(add2(ps[0], ps[1]), add2(ps[2], ps[3]));
+          l += f2lo(s2) + f2hi(s2);
+          lr += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+        }
 #pragma unroll
         for (int c = 0; c < BN / 64; ++c) tmem_st32(sbase + c * 32, p + c * 32);
         tmem_st_wait();
@@ -258,7 +251,6 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         const uint32_t tl = t + n - 1;
         if (!mbar_wait(&bars->pvdone[tl & 1][rb], (tl >> 1) & 1, abort)) goto done;
         tc_fence_after();
-        if (C::kSumMma) lr = __uint_as_float(tmem_ld1(tmem + lane_base + C::kSumCol + rb * 16));
         const float inv = 1.f / lr;
         const uint32_t obase = tmem + lane_base + C::kOCol + rb * D;
 #pragma unroll
@@ -298,7 +290,6 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16(128, BN, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
-      constexpr uint32_t kIdescSum = idesc_bf16(128, 16, false, false);
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
       // Descriptor halves: the high words are constant, the low word holds the
       // start address in 16-byte units (tiles lie below 256 KB of shared memory,
@@ -308,9 +299,6 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
       const uint32_t q_lo = static_cast<uint32_t>(dq), q_hi = static_cast<uint32_t>(dq >> 32);
       const uint32_t k_lo = static_cast<uint32_t>(dk), k_hi = static_cast<uint32_t>(dk >> 32);
       const uint32_t v_lo = static_cast<uint32_t>(dv), v_hi = static_cast<uint32_t>(dv >> 32);
-      // 16 x 16 ones, no swizzle: 8x16-byte core matrices, 128 B / 256 B apart
-      const uint64_t ones_desc = plain_desc(smem_u32(sOnes), 128, 256);
-      const uint32_t o_lo = static_cast<uint32_t>(ones_desc), o_hi = static_cast<uint32_t>(ones_desc >> 32);
       uint32_t t = 0, un = 0;
       bool ok = true;
       // O += P V for tile tt (first: overwrite O).
@@ -330,13 +318,6 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ts_w(d_tmem, a_tmem + kk * 8, vs_lo + ((kk * 2048) >> 4), v_hi, kIdescPV,
                      (!first || kk > 0) ? 1u : 0u);
-          if (C::kSumMma) {
-            // row sums of the bf16 P: P x ones, accumulated like O
-            const uint32_t d_sum = tmem + C::kSumCol + rb * 16;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ts_w(d_sum, a_tmem + kk * 8, o_lo, o_hi, kIdescSum, (!first || kk > 0) ? 1u : 0u);
-          }
           mma_commit(&bars->pvdone[b][rb]);
         }
         mma_commit(&bars->vempty[s]);
@@ -349,6 +330,17 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         const uint32_t n = static_cast<uint32_t>((len + BN - 1) / BN);
         if (n == 0) continue;
         if (!mbar_wait(&bars->qfull, un & 1, abort)) break;
+        if (C::kQTmem) {
+          // Q into TMEM, then the shared-memory copy is free for the next unit.
+          tc_fence_after();
+#pragma unroll
+          for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              tmem_cp_128x256b(tmem + C::kQCol + rb * (D / 2) + kk * 8,
+                               q_lo + ((rb * C::kQBlock + (kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4), q_hi);
+          mma_commit(&bars->qempty);
+        }
         for (uint32_t j = 0; j < n && ok; ++j) {
           const uint32_t tt = t + j, s = tt % STAGES, b = tt & 1;
           if (!mbar_wait(&bars->kfull[s], (tt / STAGES) & 1, abort)) { ok = false; break; }
@@ -359,14 +351,19 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           for (int rb = 0; rb < RB; ++rb) {
             const uint32_t d_tmem = tmem + b * C::kSCols + rb * BN;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss_w(d_tmem, q_lo + ((rb * C::kQBlock + (kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4), q_hi,
-                       ks_lo + (((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4), k_hi, kIdescS,
-                       kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t kb_lo = ks_lo + (((kk >> 2) * BN * 128 + (kk & 3) * 32) >> 4);
+              if (C::kQTmem)
+                mma_ts_w(d_tmem, tmem + C::kQCol + rb * (D / 2) + kk * 8, kb_lo, k_hi, kIdescS,
+                         kk > 0 ? 1u : 0u);
+              else
+                mma_ss_w(d_tmem, q_lo + ((rb * C::kQBlock + (kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4),
+                         q_hi, kb_lo, k_hi, kIdescS, kk > 0 ? 1u : 0u);
+            }
             mma_commit(&bars->sfull[b][rb]);
           }
           mma_commit(&bars->kempty[s]);
-          if (j == n - 1) mma_commit(&bars->qempty);
+          if (!C::kQTmem && j == n - 1) mma_commit(&bars->qempty);
           if (j >= 1 && !pv(tt - 1, j == 1)) ok = false;
         }
         if (ok && !pv(t + n - 1, n == 1)) ok = false;
@@ -393,9 +390,12 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
     uint32_t t = 0, un = 0;
     bool bad_index = false;
-    int idx_cur[C::kKVRowsPerThread], idx_nxt[C::kKVRowsPerThread], idx_prv[C::kKVRowsPerThread];
+    // Three index buffers in rotation: tile j's K copies read buffer j mod 3,
+    // its V copies (one step later) the same buffer, and tile j+1's indices
+    // load into buffer (j+1) mod 3 a whole step before they are first used.
+    int ia[C::kKVRowsPerThread], ib[C::kKVRowsPerThread], ic[C::kKVRowsPerThread];
 #pragma unroll
-    for (int i = 0; i < C::kKVRowsPerThread; ++i) idx_cur[i] = idx_nxt[i] = idx_prv[i] = 0;
+    for (int i = 0; i < C::kKVRowsPerThread; ++i) ia[i] = ib[i] = ic[i] = 0;
     for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
       int64_t begin;
       bool bad;
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
             cp_async16(dst_base + sw128_offset(r, sub + 8 * c, BN), src + 64 * c, ok ? 16u : 0u);
         }
       };
-      load_indices(0, idx_cur);
+      load_indices(0, ia);
       if (pt == 0) {
         // query rows g*M .. g*M + 128*RB - 1 of this head (rows past the
         // group feed only rows that are never written; past the tensor: zeros)
@@ -444,27 +444,30 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
             tma_load_2d(q_addr + rb * C::kQBlock + cb * 128 * 128, &tmq, 64 * cb,
                         static_cast<int>(bh * a.Nq + g * a.M + rb * 128), &bars->qfull);
       }
-      for (uint32_t j = 0; j <= n; ++j) {
+      auto step = [&](uint32_t j, const int* kb, const int* vb, int* nb) -> bool {
         const uint32_t tt = t + j;
         if (j < n) {
-          if (j + 1 < n) load_indices(j + 1, idx_nxt);
+          if (j + 1 < n) load_indices(j + 1, nb);
           const uint32_t s = tt % STAGES;
-          if (!mbar_wait(&bars->kempty[s], ((tt / STAGES) & 1) ^ 1, abort)) goto done;
-          issue(j, idx_cur, k_addr + s * C::kTile, kh, a.k);
+          if (!mbar_wait(&bars->kempty[s], ((tt / STAGES) & 1) ^ 1, abort)) return false;
+          issue(j, kb, k_addr + s * C::kTile, kh, a.k);
           cp_async_arrive_noinc(&bars->kfull[s]);
         }
         if (j >= 1) {
           const uint32_t tp = tt - 1, s = tp % STAGES;
-          if (!mbar_wait(&bars->vempty[s], ((tp / STAGES) & 1) ^ 1, abort)) goto done;
-          issue(j - 1, idx_prv, v_addr + s * C::kTile, vh, a.v);
+          if (!mbar_wait(&bars->vempty[s], ((tp / STAGES) & 1) ^ 1, abort)) return false;
+          issue(j - 1, vb, v_addr + s * C::kTile, vh, a.v);
           cp_async_arrive_noinc(&bars->vfull[s]);
         }
-#pragma unroll
-        for (int i = 0; i < C::kKVRowsPerThread; ++i) {
-          idx_prv[i] = idx_cur[i];
-          idx_cur[i] = idx_nxt[i];
-        }
+        return true;
+      };
+      bool ok = true;
+      for (uint32_t j = 0; j <= n && ok; j += 3) {
+        ok = step(j, ia, ic, ib);
+        if (ok && j + 1 <= n) ok = step(j + 1, ib, ia, ic);
+        if (ok && j + 2 <= n) ok = step(j + 2, ic, ib, ia);
       }
+      if (!ok) goto done;
       t += n;
       ++un;
     }
