@@ -118,15 +118,18 @@ struct ScoreArgs {
 
 template <int D>
 struct ScoreCfg {
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 3;
   static constexpr int kThreads = 32 * 6;  // 4 epilogue warps, 1 MMA warp, 1 TMA warp
   static constexpr int kTile = 128 * D * 2;  // 128 rows of d bf16
-  static constexpr int kSmemBytes = 1024 + 2 * kTile + kStages * kTile + 1024;
+  // Each epilogue warp stages its 32 keys x 128 rows of fp32 scores (16 KB)
+  // and writes them with one TMA store.
+  static constexpr int kOutSlab = 32 * 128 * 4;
+  static constexpr int kSmemBytes = 1024 + 2 * kTile + kStages * kTile + 4 * kOutSlab + 1024;
   static constexpr int kTmemCols = 256;
 };
 
 struct ScoreBars {
-  uint64_t kfull[4], kempty[4];
+  uint64_t kfull[3], kempty[3];
   uint64_t qfull, qempty, drain;
   uint64_t dfull[2], dempty[2];
   uint32_t tmem_base;
@@ -147,7 +150,8 @@ __device__ __forceinline__ void score_unit(const ScoreArgs& a, int64_t u, int64_
 template <int D>
 __global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1)
     sa_score_kernel(const ScoreArgs a, const __grid_constant__ CUtensorMap tm_qhi,
-                    const __grid_constant__ CUtensorMap tm_qlo, const __grid_constant__ CUtensorMap tm_k) {
+                    const __grid_constant__ CUtensorMap tm_qlo, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_out) {
   using C = ScoreCfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -155,7 +159,8 @@ __global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1)
   uint8_t* sQh = smem;
   uint8_t* sQl = sQh + C::kTile;
   uint8_t* sK = sQl + C::kTile;
-  ScoreBars* bars = reinterpret_cast<ScoreBars*>(sK + S * C::kTile);
+  uint8_t* sOut = sK + S * C::kTile;
+  ScoreBars* bars = reinterpret_cast<ScoreBars*>(sOut + 4 * C::kOutSlab);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -184,15 +189,16 @@ __global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1)
 
   if (warp < 4) {
     // ------------------------------------------------------------ epilogue
+    // Lane = key: the warp's 32 keys x 128 mean-query rows go to its slab as
+    // [row][key] and leave with one TMA store (clipped at Nk and at G).
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float* slab = reinterpret_cast<float*>(sOut + warp * C::kOutSlab);
+    const uint32_t slab_addr = smem_u32(slab);
     uint32_t t = 0;
     for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
       int64_t bh;
       int gc, t0, t1;
       score_unit(a, u, &bh, &gc, &t0, &t1);
-      const int64_t g0 = int64_t(gc) * 128;
-      const int ng = static_cast<int>(min64(128, a.G - g0));
-      float* dst0 = a.scores + (bh * a.G + g0) * a.ld;
       for (int tile = t0; tile < t1; ++tile, ++t) {
         const uint32_t b = t & 1;
         if (!mbar_wait(&bars->dfull[b], (t >> 1) & 1, abort)) goto done;
@@ -204,12 +210,16 @@ __global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&bars->dempty[b]);
-        const int64_t key = int64_t(tile) * 128 + warp * 32 + lane;
-        if (key < a.Nk) {
-          float* dst = dst0 + key;
+        // the previous tile's store must have read the slab
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
 #pragma unroll
-          for (int gi = 0; gi < 128; ++gi)
-            if (gi < ng) dst[int64_t(gi) * a.ld] = x[gi] * a.scale;
+        for (int gi = 0; gi < 128; ++gi) slab[gi * 32 + lane] = x[gi] * a.scale;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_out, slab_addr, tile * 128 + warp * 32, gc * 128, static_cast<int>(bh));
+          bulk_commit();
         }
       }
     }
@@ -290,6 +300,8 @@ __global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1)
     }
   }
 done:
+  // score stores must be complete (and off the slabs) before the block exits
+  if (warp < 4 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && bars->abort) report(a.status, SA_DEVERR_TIMEOUT);
@@ -1089,16 +1101,18 @@ static cudaError_t launch_scores(const BuildArgs& a, int num_sms, cudaStream_t s
   s.units = base * s.ksplit;
   s.scale = a.scale;
   s.status = status;
-  CUtensorMap tm_qhi, tm_qlo, tm_k;
+  CUtensorMap tm_qhi, tm_qlo, tm_k, tm_out;
   if (!make_rows_map(&tm_qhi, s.qhi, uint64_t(a.rows), D, 128) ||
       !make_rows_map(&tm_qlo, s.qlo, uint64_t(a.rows), D, 128) ||
-      !make_rows_map(&tm_k, a.k, uint64_t(a.BH) * a.Nk, D, 128))
+      !make_rows_map(&tm_k, a.k, uint64_t(a.BH) * a.Nk, D, 128) ||
+      !make_scores_map(&tm_out, s.scores, static_cast<uint32_t>(a.Nk), uint64_t(a.G), uint64_t(a.BH),
+                       uint64_t(s.ld)))
     return cudaErrorInvalidValue;
   auto kern = sa_score_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t grid = s.units < num_sms ? s.units : num_sms;
-  kern<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, st>>>(s, tm_qhi, tm_qlo, tm_k);
+  kern<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, st>>>(s, tm_qhi, tm_qlo, tm_k, tm_out);
   return cudaGetLastError();
 }
 

@@ -44,4 +44,21 @@ inline bool make_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The fp32 score matrix of B*H heads x G rows x Nk keys (row stride ld
+// floats, head stride G*ld floats) seen as boxes of 32 keys x 128 rows of one
+// head, unswizzled.  Stores clip at Nk, at G (never into the next head) and
+// at the last head.
+inline bool make_scores_map(CUtensorMap* map, void* base, uint32_t Nk, uint64_t G, uint64_t BH,
+                            uint64_t ld) {
+  const EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {Nk, G, BH};
+  const cuuint64_t strides[2] = {ld * 4, G * ld * 4};
+  const cuuint32_t box[3] = {32, 128, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace sa
