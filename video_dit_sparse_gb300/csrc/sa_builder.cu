@@ -325,9 +325,11 @@ struct SelArgs {
   int64_t* counts;
   int32_t* col_idx;      // TOPK only: lists are emitted by the select kernel
   int64_t col_capacity;
+  int32_t mask_words;    // TOPK: words of the kept-key bitmask (0: emit by re-reading the row)
 };
 
 constexpr int kSelThreads = 256;            // one row per block, 4 blocks resident per SM
+constexpr size_t kSelSmemBudget = 56 * 1024;  // dynamic shared memory per block for 4 blocks per SM
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kBins = 1024;                 // linear bins over the undecided score range
 constexpr int kBinsPerThread = kBins / kSelThreads;
@@ -729,9 +731,36 @@ __device__ void emit_row(const float* s, int Nk, uint32_t ck, int64_t nt, int64_
   }
 }
 
-__global__ void __launch_bounds__(kSelThreads) sa_select_kernel(const SelArgs a) {
+__device__ __forceinline__ bool by_mass_mode(const SelArgs& a) { return a.mode != SA_SELECT_TOPK; }
+
+// Writes the indices of the set bits of kept[0, words) in ascending order to
+// col_idx[base, ...): each thread owns a run of words, the runs' offsets come
+// from one block scan of their popcounts.
+__device__ void emit_mask(const uint32_t* kept, int words, int64_t base, int32_t* col_idx,
+                          int64_t* scratch) {
+  const int per = (words + kSelThreads - 1) / kSelThreads;
+  const int w0 = min(words, static_cast<int>(threadIdx.x) * per), w1 = min(words, w0 + per);
+  int64_t n = 0;
+  for (int w = w0; w < w1; ++w) n += __popc(kept[w]);
+  int64_t total;
+  int64_t pos = base + block_excl_scan<int64_t>(n, &total, scratch);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bits = kept[w];
+    while (bits) {
+      const int bit = __ffs(bits) - 1;
+      col_idx[pos++] = w * 32 + bit;
+      bits &= bits - 1;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs a) {
   extern __shared__ uint8_t sel_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(sel_raw);
+  // TOPK: bit j of kept[j / 32] marks key j as kept (keys above the bracket
+  // during the window pass, kept keys of the window after the selection).
+  uint32_t* kept = reinterpret_cast<uint32_t*>(sel_raw + sizeof(SelSmem));
+  const bool use_mask = !by_mass_mode(a) && a.col_idx && a.mask_words > 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.x;
   const float* s = a.scores + row * a.ld;
@@ -906,7 +935,7 @@ __global__ void __launch_bounds__(kSelThreads) sa_select_kernel(const SelArgs a)
         }
         if (b >= nv && (4 * b >= Nk)) break;
         int n_in = 0;
-        uint32_t in_mask = 0;
+        uint32_t in_mask = 0, above_bits = 0;
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
@@ -916,6 +945,7 @@ __global__ void __launch_bounds__(kSelThreads) sa_select_kernel(const SelArgs a)
             const bool above = valid && xv > hi;
             const bool inw = valid && xv >= lo && xv <= hi;
             c_above += above;
+            above_bits |= (above ? 1u : 0u) << (u * 4 + e);
             if (by_mass && (above || inw)) {
               const unsigned long long fm = fixed_mass(xv, rmax);
               if (above) m_above += fm;
@@ -924,6 +954,18 @@ __global__ void __launch_bounds__(kSelThreads) sa_select_kernel(const SelArgs a)
             in_mask |= (inw ? 1u : 0u) << (u * 4 + e);
             n_in += inw;
           }
+        if (use_mask) {
+          // eight lanes hold the 32 keys of one mask word: OR their nibbles
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            uint32_t w = ((above_bits >> (u * 4)) & 0xFu) << (4 * (lane & 7));
+            w |= __shfl_xor_sync(0xffffffffu, w, 1);
+            w |= __shfl_xor_sync(0xffffffffu, w, 2);
+            w |= __shfl_xor_sync(0xffffffffu, w, 4);
+            const int word = (b + u * 32 + lane) >> 3;
+            if ((lane & 7) == 0 && word < a.mask_words) kept[word] = w;
+          }
+        }
         // warp-aggregated append of this lane's in-bracket keys
         int pre = n_in;
 #pragma unroll
@@ -980,11 +1022,31 @@ __global__ void __launch_bounds__(kSelThreads) sa_select_kernel(const SelArgs a)
       exact_select(RowSrc{s, Nk}, mn, mx, k, target, by_mass, rmax, 0, 0, Nk, sm, &cut, &ties, &count);
     }
     if (!by_mass && a.col_idx) {
-      // TOPK: every row holds exactly k keys, so row r starts at r*k and
-      // the lists are written here while the row is still in L2.
+      // TOPK: every row holds exactly k keys, so row r starts at r*k.
       const int64_t base = row * k;
-      if (base + k <= a.col_capacity)
-        emit_row(s, Nk, cut, ties, base, base + k, a.col_idx, sm.seg_sel, sm.seg_tie);
+      if (base + k <= a.col_capacity) {
+        // The bitmask serves when the cut fell in the bracket and keeps all of
+        // its ties (every key equal to the cut lies in the window); else the
+        // row is read again.
+        bool from_mask = use_mask && bracketed;
+        if (from_mask) {
+          int nt = 0;
+          for (int i = tid; i < n_win; i += kSelThreads) nt += order_key(sm.u.win.x[i]) == cut;
+          int64_t nt_all;
+          block_excl_scan<int64_t>(nt, &nt_all, sm.scan_c);
+          from_mask = nt_all == ties;
+        }
+        if (from_mask) {
+          for (int i = tid; i < n_win; i += kSelThreads) {
+            const int j = sm.u.win.j[i];
+            if (order_key(sm.u.win.x[i]) >= cut) atomicOr(&kept[j >> 5], 1u << (j & 31));
+          }
+          __syncthreads();
+          emit_mask(kept, a.mask_words, base, a.col_idx, sm.scan_c);
+        } else {
+          emit_row(s, Nk, cut, ties, base, base + k, a.col_idx, sm.seg_sel, sm.seg_tie);
+        }
+      }
     }
   }
   if (tid == 0) {
@@ -1143,10 +1205,15 @@ cudaError_t launch_build_index(const BuildArgs& a, int num_sms, cudaStream_t st)
   s.counts = reinterpret_cast<int64_t*>(a.ws + a.L.counts);
   s.col_idx = a.mode == SA_SELECT_TOPK ? a.col_idx : nullptr;
   s.col_capacity = a.col_capacity;
+  // TOPK lists come from a kept-key bitmask in shared memory while four
+  // blocks still fit on an SM; longer rows are read a second time instead.
+  const int words = (a.Nk + 31) / 32;
+  s.mask_words = (a.mode == SA_SELECT_TOPK && sizeof(SelSmem) + size_t(words) * 4 <= kSelSmemBudget) ? words : 0;
+  const size_t sel_smem = sizeof(SelSmem) + size_t(s.mask_words) * 4;
   e = cudaFuncSetAttribute(sa_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sizeof(SelSmem)));
+                           static_cast<int>(sel_smem));
   if (e != cudaSuccess) return e;
-  sa_select_kernel<<<static_cast<unsigned>(a.rows), kSelThreads, sizeof(SelSmem), st>>>(s);
+  sa_select_kernel<<<static_cast<unsigned>(a.rows), kSelThreads, sel_smem, st>>>(s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   sa_scan_kernel<<<1, 1024, 0, st>>>(s.counts, a.rows, a.row_ptr, misc, a.col_capacity, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
