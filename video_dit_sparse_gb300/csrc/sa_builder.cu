@@ -329,14 +329,15 @@ struct SelArgs {
 };
 
 constexpr int kSelThreads = 256;            // one row per block, 4 blocks resident per SM
-constexpr size_t kSelSmemBudget = 56 * 1024;  // dynamic shared memory per block for 4 blocks per SM
+constexpr size_t kSelSmemBudget = 75 * 1024;  // dynamic shared memory per block: 3 or 4 blocks per SM
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kBins = 1024;                 // linear bins over the undecided score range
 constexpr int kBinsPerThread = kBins / kSelThreads;
 constexpr int kLevels = 3;                  // bin refinements of the crossing bin
 constexpr int kRank = 512;                  // exact ranking once this few keys are undecided
-constexpr int kWindow = 4096;               // keys the sampled bracket may hold
-constexpr int kSampleMax = 2 * kWindow;     // samples share the bracket's storage
+constexpr int kWindow = 8192;               // keys the sampled bracket may hold (indices)
+constexpr int kSampleMax = kWindow;         // samples share the bracket's storage
+constexpr int kNoSample = 4096;             // rows this short are selected without a sample
 constexpr int kUnroll = 4;                  // float4 loads in flight per lane
 constexpr int kWinUnroll = 4;               // ... in the bracket pass (16 keys per lane)
 constexpr float kMassOne = 4294967296.0f;   // fixed-point unit of probability mass (2^32)
@@ -366,7 +367,6 @@ struct SelSmem {
   int32_t rj[kRank];
   union {
     struct {
-      float x[kWindow];
       int32_t j[kWindow];
     } win;
     float sample[kSampleMax];
@@ -387,11 +387,13 @@ struct RowSrc {
   __device__ __forceinline__ float x(int i) const { return s[i]; }
   __device__ __forceinline__ int j(int i) const { return i; }
 };
-struct WinSrc {
-  const float* xs;
+// Keys of the bracketed window: indices in shared memory, scores re-read
+// from the row (in L2 after the window pass).
+struct RowIdxSrc {
+  const float* s;
   const int32_t* js;
   int n;
-  __device__ __forceinline__ float x(int i) const { return xs[i]; }
+  __device__ __forceinline__ float x(int i) const { return s[js[i]]; }
   __device__ __forceinline__ int j(int i) const { return js[i]; }
 };
 
@@ -826,7 +828,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
     }
     // ---- bracket the cut from an evenly strided sample of the row
     float lo = -INFINITY, hi = INFINITY;
-    if (Nk > kWindow) {
+    if (Nk > kNoSample) {
       const int S = Nk / 4 < kSampleMax ? (Nk / 4 > 1024 ? Nk / 4 : 1024) : kSampleMax;
       const int stride = Nk / S;  // >= 1: samples j = i*stride, evenly spread over the row
       float smn = INFINITY, smx = -INFINITY;
@@ -983,7 +985,6 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
           for (int e = 0; e < 4; ++e)
             if (in_mask >> (u * 4 + e) & 1u) {
               if (slot < kWindow) {
-                sm.u.win.x[slot] = x[u][e];
                 sm.u.win.j[slot] = jb[u] + e;
               }
               ++slot;
@@ -1003,12 +1004,13 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
     if (bracketed) {
       float wmn = INFINITY, wmx = -INFINITY;
       for (int i = tid; i < n_win; i += kSelThreads) {
-        wmn = fminf(wmn, sm.u.win.x[i]);
-        wmx = fmaxf(wmx, sm.u.win.x[i]);
+        const float xv = s[sm.u.win.j[i]];
+        wmn = fminf(wmn, xv);
+        wmx = fmaxf(wmx, xv);
       }
       wmn = block_min(wmn, sm);
       wmx = block_max(wmx, sm);
-      exact_select(WinSrc{sm.u.win.x, sm.u.win.j, n_win}, wmn, wmx, k, target, by_mass, rmax, above_cnt,
+      exact_select(RowIdxSrc{s, sm.u.win.j, n_win}, wmn, wmx, k, target, by_mass, rmax, above_cnt,
                    above_mass, Nk, sm, &cut, &ties, &count);
     } else {
       // The sample missed (or the bracket overflowed): select over the row.
@@ -1031,7 +1033,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
         bool from_mask = use_mask && bracketed;
         if (from_mask) {
           int nt = 0;
-          for (int i = tid; i < n_win; i += kSelThreads) nt += order_key(sm.u.win.x[i]) == cut;
+          for (int i = tid; i < n_win; i += kSelThreads) nt += order_key(s[sm.u.win.j[i]]) == cut;
           int64_t nt_all;
           block_excl_scan<int64_t>(nt, &nt_all, sm.scan_c);
           from_mask = nt_all == ties;
@@ -1039,7 +1041,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
         if (from_mask) {
           for (int i = tid; i < n_win; i += kSelThreads) {
             const int j = sm.u.win.j[i];
-            if (order_key(sm.u.win.x[i]) >= cut) atomicOr(&kept[j >> 5], 1u << (j & 31));
+            if (order_key(s[j]) >= cut) atomicOr(&kept[j >> 5], 1u << (j & 31));
           }
           __syncthreads();
           emit_mask(kept, a.mask_words, base, a.col_idx, sm.scan_c);
@@ -1205,8 +1207,8 @@ cudaError_t launch_build_index(const BuildArgs& a, int num_sms, cudaStream_t st)
   s.counts = reinterpret_cast<int64_t*>(a.ws + a.L.counts);
   s.col_idx = a.mode == SA_SELECT_TOPK ? a.col_idx : nullptr;
   s.col_capacity = a.col_capacity;
-  // TOPK lists come from a kept-key bitmask in shared memory while four
-  // blocks still fit on an SM; longer rows are read a second time instead.
+  // TOPK lists come from a kept-key bitmask in shared memory (rows up to
+  // ~200K keys); longer rows are read a second time instead.
   const int words = (a.Nk + 31) / 32;
   s.mask_words = (a.mode == SA_SELECT_TOPK && sizeof(SelSmem) + size_t(words) * 4 <= kSelSmemBudget) ? words : 0;
   const size_t sel_smem = sizeof(SelSmem) + size_t(s.mask_words) * 4;
