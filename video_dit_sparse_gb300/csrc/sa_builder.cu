@@ -917,13 +917,13 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
       const int nv = Nk >> 2;
       const float4* s4 = reinterpret_cast<const float4*>(s);
       constexpr int U = kWinUnroll;
+      // Keys past the row read as NaN: every comparison with them is false.
+      const float nan = __int_as_float(0x7fffffff);
       for (int b = warp * 32 * U; b < nv + 32 * U; b += kSelThreads * U) {
         float x[U][4];
-        int jb[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int i4 = b + u * 32 + lane;
-          jb[u] = 4 * i4;
           if (i4 < nv) {
             const float4 v = __ldg(s4 + i4);
             x[u][0] = v.x;
@@ -932,30 +932,29 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
             x[u][3] = v.w;
           } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[u][e] = 4 * i4 + e < Nk ? s[4 * i4 + e] : -INFINITY;
+            for (int e = 0; e < 4; ++e) x[u][e] = 4 * i4 + e < Nk ? s[4 * i4 + e] : nan;
           }
         }
         if (b >= nv && (4 * b >= Nk)) break;
-        int n_in = 0;
+        // bit u*4+e: key 4*(b + 32u + lane) + e
         uint32_t in_mask = 0, above_bits = 0;
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float xv = x[u][e];
-            const bool valid = jb[u] + e < Nk;
-            const bool above = valid && xv > hi;
-            const bool inw = valid && xv >= lo && xv <= hi;
-            c_above += above;
+            const bool above = xv > hi;
+            const bool inw = xv >= lo && !above;
             above_bits |= (above ? 1u : 0u) << (u * 4 + e);
+            in_mask |= (inw ? 1u : 0u) << (u * 4 + e);
             if (by_mass && (above || inw)) {
               const unsigned long long fm = fixed_mass(xv, rmax);
               if (above) m_above += fm;
               else m_win += fm;
             }
-            in_mask |= (inw ? 1u : 0u) << (u * 4 + e);
-            n_in += inw;
           }
+        c_above += __popc(above_bits);
+        const int n_in = __popc(in_mask);
         if (use_mask) {
           // eight lanes hold the 32 keys of one mask word: OR their nibbles
 #pragma unroll
@@ -976,19 +975,14 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
           if (lane >= o) pre += t;
         }
         const int tot = __shfl_sync(0xffffffffu, pre, 31);
+        if (tot == 0) continue;
         int slot0 = 0;
-        if (lane == 0 && tot) slot0 = atomicAdd(&sm.n_win, tot);
+        if (lane == 0) slot0 = atomicAdd(&sm.n_win, tot);
         int slot = __shfl_sync(0xffffffffu, slot0, 0) + pre - n_in;
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (in_mask >> (u * 4 + e) & 1u) {
-              if (slot < kWindow) {
-                sm.u.win.j[slot] = jb[u] + e;
-              }
-              ++slot;
-            }
+        for (uint32_t m = in_mask; m; m &= m - 1, ++slot) {
+          const int bit = __ffs(m) - 1;
+          if (slot < kWindow) sm.u.win.j[slot] = 4 * (b + (bit >> 2) * 32 + lane) + (bit & 3);
+        }
       }
     }
     int64_t above_cnt, above_mass = 0, win_mass = 0;
