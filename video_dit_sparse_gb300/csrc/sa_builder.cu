@@ -389,6 +389,13 @@ struct RowSrc {
 };
 // Keys of the bracketed window: indices in shared memory, scores re-read
 // from the row (in L2 after the window pass).
+struct WinSrc {
+  const float* xs;
+  const int32_t* js;
+  int n;
+  __device__ __forceinline__ float x(int i) const { return xs[i]; }
+  __device__ __forceinline__ int j(int i) const { return js[i]; }
+};
 struct RowIdxSrc {
   const float* s;
   const int32_t* js;
@@ -995,17 +1002,26 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
     const bool bracketed =
         n_win <= kWindow && (by_mass ? (double(above_mass) < target && target <= double(above_mass + win_mass))
                                      : (above_cnt < k && k <= above_cnt + n_win));
+    // A window of at most kWindow/2 keys gets its scores copied next to the
+    // indices (one gather from L2), so the selection passes read shared memory.
+    const bool win_x = n_win <= kWindow / 2;
+    float* wx = reinterpret_cast<float*>(sm.u.win.j + kWindow / 2);
     if (bracketed) {
       float wmn = INFINITY, wmx = -INFINITY;
       for (int i = tid; i < n_win; i += kSelThreads) {
         const float xv = s[sm.u.win.j[i]];
+        if (win_x) wx[i] = xv;
         wmn = fminf(wmn, xv);
         wmx = fmaxf(wmx, xv);
       }
-      wmn = block_min(wmn, sm);
+      wmn = block_min(wmn, sm);  // (its barriers also publish wx)
       wmx = block_max(wmx, sm);
-      exact_select(RowIdxSrc{s, sm.u.win.j, n_win}, wmn, wmx, k, target, by_mass, rmax, above_cnt,
-                   above_mass, Nk, sm, &cut, &ties, &count);
+      if (win_x)
+        exact_select(WinSrc{wx, sm.u.win.j, n_win}, wmn, wmx, k, target, by_mass, rmax, above_cnt,
+                     above_mass, Nk, sm, &cut, &ties, &count);
+      else
+        exact_select(RowIdxSrc{s, sm.u.win.j, n_win}, wmn, wmx, k, target, by_mass, rmax, above_cnt,
+                     above_mass, Nk, sm, &cut, &ties, &count);
     } else {
       // The sample missed (or the bracket overflowed): select over the row.
       float mn = INFINITY, mx = -INFINITY;
@@ -1027,7 +1043,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
         bool from_mask = use_mask && bracketed;
         if (from_mask) {
           int nt = 0;
-          for (int i = tid; i < n_win; i += kSelThreads) nt += order_key(s[sm.u.win.j[i]]) == cut;
+          for (int i = tid; i < n_win; i += kSelThreads)
+            nt += order_key(win_x ? wx[i] : s[sm.u.win.j[i]]) == cut;
           int64_t nt_all;
           block_excl_scan<int64_t>(nt, &nt_all, sm.scan_c);
           from_mask = nt_all == ties;
@@ -1035,7 +1052,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
         if (from_mask) {
           for (int i = tid; i < n_win; i += kSelThreads) {
             const int j = sm.u.win.j[i];
-            if (order_key(s[j]) >= cut) atomicOr(&kept[j >> 5], 1u << (j & 31));
+            if (order_key(win_x ? wx[i] : s[j]) >= cut) atomicOr(&kept[j >> 5], 1u << (j & 31));
           }
           __syncthreads();
           emit_mask(kept, a.mask_words, base, a.col_idx, sm.scan_c);
