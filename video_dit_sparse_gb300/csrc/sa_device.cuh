@@ -98,6 +98,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ registers
+// Per-warpgroup register reallocation (every warp of an aligned group of four
+// executes it with the same count).  An increase draws on registers that other
+// warpgroups released; the launch's registers bound the sum.
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ TMA
 // Arrive on `bar` (count 1) and add `bytes` to the transaction count that
 // the TMA copies of this phase will complete.

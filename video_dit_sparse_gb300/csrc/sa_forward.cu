@@ -34,9 +34,17 @@ struct FwdCfg {
   static constexpr int kSoftmaxWarps = 4 * RB;
   static constexpr int kMmaWarp = kSoftmaxWarps;
   static constexpr int kProdWarp0 = kSoftmaxWarps + 1;
-  static constexpr int kProdWarps = 3;
+  // 128-row groups: seven gather warps (12 warps in all), with the softmax
+  // warpgroup's registers raised and the rest lowered after launch; 192-row
+  // groups: three (their eight softmax warps fill the register file).
+  static constexpr int kProdWarps = RB == 1 ? 7 : 3;
   static constexpr int kProdThreads = 32 * kProdWarps;
   static constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProdWarps);
+  static constexpr bool kRegSplit = RB == 1;
+  static constexpr int kRegSoftmax = 240, kRegOther = 80;
+  static_assert(!kRegSplit || (kRegSoftmax * 4 + kRegOther * (kThreads / 32 - 4)) * 32 <=
+                                  (65536 / kThreads / 8 * 8) * kThreads,
+                "register split exceeds the launch's registers");
   // Gather mapping: 8 lanes per row, lane copies 16-byte chunks sub, sub+8
   // (one 128-byte line of 4 rows per copy instruction).
   static constexpr int kLanesPerRow = 8;
@@ -131,6 +139,12 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const int64_t G = a.G;
+  if (C::kRegSplit) {
+    if (warp < 4)
+      reg_alloc<C::kRegSoftmax>();
+    else
+      reg_dealloc<C::kRegOther>();
+  }
 
   if (warp < C::kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax
