@@ -401,6 +401,12 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     const int pt = threadIdx.x - C::kProdWarp0 * 32;
     const int sub = pt % C::kLanesPerRow;
     const int row0 = pt / C::kLanesPerRow;
+    // shared-memory offset of chunk `sub` of each of this thread's rows (the
+    // chunks sub + 8c lie c column blocks further on)
+    uint32_t dst_off[C::kKVRowsPerThread];
+#pragma unroll
+    for (int i = 0; i < C::kKVRowsPerThread; ++i)
+      dst_off[i] = sw128_offset(row0 + i * C::kRowStep, sub, BN);
     const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
     uint32_t t = 0, un = 0;
     bool bad_index = false;
@@ -431,18 +437,20 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
       // outside [0, Nk), are zero-filled.
       auto issue = [&](uint32_t jj, const int* idx, uint32_t dst_base, const uint16_t* src_head,
                        const uint16_t* any) {
+        const int64_t rem = len - int64_t(jj) * BN;  // list rows from this tile on
+        const int lim = rem < BN ? static_cast<int>(rem) : BN;
 #pragma unroll
         for (int i = 0; i < C::kKVRowsPerThread; ++i) {
           const int r = row0 + i * C::kRowStep;
           if (r >= BN) break;
-          const int64_t pos = int64_t(jj) * BN + r;
-          const bool in_list = pos < len;
+          const bool in_list = r < lim;
           const bool ok = in_list && static_cast<uint32_t>(idx[i]) < static_cast<uint32_t>(a.Nk);
           bad_index |= in_list && !ok;
           const uint16_t* src = ok ? src_head + int64_t(idx[i]) * D : any;
+          const uint32_t dst = dst_base + dst_off[i];
 #pragma unroll
           for (int c = 0; c < C::kChunksPerLane; ++c)
-            cp_async16(dst_base + sw128_offset(r, sub + 8 * c, BN), src + 64 * c, ok ? 16u : 0u);
+            cp_async16(dst + c * BN * 128, src + 64 * c, ok ? 16u : 0u);
         }
       };
       load_indices(0, ia);
