@@ -5,7 +5,10 @@ check and by the benchmark's CPU-baseline leg, never by the product path.
 The arithmetic lives in ``oracle.c``; this file only marshals numpy arrays.
 It shares no code with the CUDA path.
 
-Modes follow the C side: 0 = TOPK, 1 = THRESHOLD, 2 = MASS.
+Modes follow the C side: 0 = TOPK, 1 = THRESHOLD, 2 = MASS, 3 = LEVEL (the
+statistic itself reaches tau; used for dense-step lists).  Column
+statistics: 0 = MAX, 1 = SUM over a group's queries of the dense-step
+attention probabilities.
 """
 from __future__ import annotations
 
@@ -19,8 +22,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-TOPK, THRESHOLD, MASS = 0, 1, 2
-MODES = {"topk": TOPK, "threshold": THRESHOLD, "mass": MASS}
+TOPK, THRESHOLD, MASS, LEVEL = 0, 1, 2, 3
+MODES = {"topk": TOPK, "threshold": THRESHOLD, "mass": MASS, "level": LEVEL}
+STAT_MAX, STAT_SUM = 0, 1
+STATS = {"max": STAT_MAX, "sum": STAT_SUM}
 
 _lib = None
 
@@ -46,8 +51,12 @@ def _configure(lib):
                                   ctypes.c_double, p, p, p, ctypes.c_int]
     lib.oracle_forward.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64,
                                    ctypes.c_double, p, p, p, i64, p, p, ctypes.c_int]
+    lib.oracle_column_stats.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64,
+                                        ctypes.c_double, ctypes.c_int, p, i64, p, ctypes.c_int]
+    lib.oracle_forward_delta.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_double,
+                                         p, p, p, p, ctypes.c_double, p, i64, p, ctypes.c_int]
     for f in (lib.oracle_mean_query, lib.oracle_group_scores, lib.oracle_select,
-              lib.oracle_forward):
+              lib.oracle_forward, lib.oracle_column_stats, lib.oracle_forward_delta):
         f.restype = ctypes.c_int
     return lib
 
@@ -172,3 +181,87 @@ def forward(q, k, v, M: int, scale: float, row_ptr, col_idx, units=None,
     if rc:
         raise ValueError("oracle_forward rejected its arguments")
     return o, lse
+
+
+def dense_lse(q, k, scale: float, M: int | None = None, units=None, threads: int | None = None):
+    """Row log-sum-exp over all Nk keys (the dense step), computed by the
+    restricted-attention oracle with every key kept.  Without `units`:
+    float64 [B, H, Nq]; with `units` (query groups of M rows): [n_units, M]."""
+    q, k = _bits(q), _bits(k)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if M is None:
+        M = Nq  # one group per head
+    G = -(-Nq // M)
+    full = units is None
+    units = _units(units, B * H * G)
+    # CSR in which each listed unit keeps every key (the others stay empty)
+    counts = np.zeros(B * H * G, dtype=np.int64)
+    counts[units] = Nk
+    row_ptr = np.zeros(B * H * G + 1, dtype=np.int64)
+    np.cumsum(counts, out=row_ptr[1:])
+    col = np.tile(np.arange(Nk, dtype=np.int32), units.size)
+    _, lse = forward(q, k, k, M, scale, row_ptr, col, units, threads)
+    if full:
+        return lse.reshape(B, H, G * M)[:, :, :Nq]
+    return lse
+
+
+def column_stats(q, k, lse, M: int, scale: float, stat, units=None, threads: int | None = None):
+    """ln of the per-key column statistic of each listed unit: float64
+    [n_units, Nk].  stat "max": max over the group's queries of
+    exp(s q.k - lse); "sum": their sum.  lse: [B, H, Nq] (any float type)."""
+    q, k = _bits(q), _bits(k)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    G = -(-Nq // M)
+    units = _units(units, B * H * G)
+    lse = np.ascontiguousarray(lse, dtype=np.float64).reshape(B, H, Nq)
+    out = np.empty((units.size, Nk), dtype=np.float64)
+    rc = _load().oracle_column_stats(_ptr(q), _ptr(k), _ptr(lse), B, H, Nq, Nk, d, M,
+                                     float(scale), int(STATS.get(stat, stat)), _ptr(units),
+                                     units.size, _ptr(out), threads or default_threads())
+    if rc:
+        raise ValueError("oracle_column_stats rejected its arguments")
+    return out
+
+
+def dense_index(q, k, lse, M: int, scale: float, stat, mode, topk: int = 0, tau: float = 0.0,
+                rho: float = 0.99, units=None, threads: int | None = None):
+    """Dense-step lists: column statistics + selection.  mode "threshold"
+    means LEVEL here (the statistic itself reaches tau).  Returns
+    (lists, cut, ln-statistics)."""
+    st = column_stats(q, k, lse, M, scale, stat, units, threads)
+    m = MODES.get(mode, mode)
+    if m == THRESHOLD:
+        m = LEVEL
+    lists, cut = select(st, m, topk, tau, rho, threads)
+    return lists, cut, st
+
+
+def forward_delta(q, k, v, M: int, scale: float, row_ptr, col_idx, lse, base=None,
+                  sign: float = 1.0, units=None, threads: int | None = None):
+    """Sparse-delta attention: o_i = base_i + sign * sum over kept j of
+    exp(s q_i.k_j - lse_i) v_j.  Returns float64 [n_units, M, d]."""
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    G = -(-Nq // M)
+    units = _units(units, B * H * G)
+    row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int64)
+    col_idx = np.ascontiguousarray(col_idx, dtype=np.int32)
+    if row_ptr.size != B * H * G + 1:
+        raise ValueError("row_ptr must have B*H*G+1 entries")
+    if col_idx.size == 0:
+        col_idx = np.zeros(1, dtype=np.int32)
+    lse = np.ascontiguousarray(lse, dtype=np.float64).reshape(B, H, Nq)
+    if base is not None:
+        base = np.ascontiguousarray(base, dtype=np.float64).reshape(B, H, Nq, d)
+    o = np.empty((units.size, M, d), dtype=np.float64)
+    rc = _load().oracle_forward_delta(_ptr(q), _ptr(k), _ptr(v), B, H, Nq, Nk, d, M, float(scale),
+                                      _ptr(row_ptr), _ptr(col_idx), _ptr(lse),
+                                      None if base is None else _ptr(base), float(sign),
+                                      _ptr(units), units.size, _ptr(o), threads or default_threads())
+    if rc:
+        raise ValueError("oracle_forward_delta rejected its arguments")
+    return o

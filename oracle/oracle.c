@@ -37,6 +37,19 @@
  *    rho >= 1, since every p_j is positive).
  *  - the reported cut is the score of the last key taken (TOPK, MASS) or
  *    ln(tau) + LSE_all (THRESHOLD).
+ *  - dense-step lists (FG-Attn review, cached mask, "free parameters" and
+ *    Fig. 10: keep a slice when at least one of its full-attention scores
+ *    reaches tau_cached = 0.5/N; Chipmunk review, major comment 2 / Alg. 4:
+ *    top-k columns by column sums of the attention probabilities, with the
+ *    softmax constants of an earlier step): per group and key, the maximum
+ *    (or the sum) over the group's queries of p_ij = exp(s q_i.k_j - lse_i),
+ *    with lse_i supplied by the caller (the dense step's row log-sum-exp);
+ *    rows whose lse is not finite contribute nothing.  The lists rank keys by
+ *    ln of that statistic; LEVEL keeps keys whose statistic reaches tau.
+ *  - sparse-delta attention (Chipmunk review, "What carries the argument",
+ *    Eq. 1 as the referee reads it, and Appendix B.2: reuse the previous
+ *    step's softmax normalisation): o_i = base_i + sign * sum over kept j of
+ *    exp(s q_i.k_j - lse_i) v_j, with lse_i supplied; no renormalisation.
  *
  * Inputs are bf16 bit patterns (uint16) in [B, H, N, d] row-major order;
  * every bf16 value converts to double exactly.
@@ -50,6 +63,9 @@
 #define ORACLE_TOPK 0
 #define ORACLE_THRESHOLD 1
 #define ORACLE_MASS 2
+#define ORACLE_LEVEL 3
+#define ORACLE_STAT_MAX 0
+#define ORACLE_STAT_SUM 1
 
 static double bf16_value(uint16_t bits) {
   uint32_t u = (uint32_t)bits << 16;
@@ -227,6 +243,11 @@ static void select_row(void* vctx, int64_t r) {
     n = c->topk < Nk ? c->topk : Nk;
     if (n < 1) n = 1;
     cut = order[n - 1].score;
+  } else if (c->mode == ORACLE_LEVEL) {
+    /* the statistic exp(score) itself reaches tau; a prefix of the ranking */
+    while (n < Nk && exp(order[n].score) >= c->tau) ++n;
+    if (n < 1) n = 1;
+    cut = log(c->tau);
   } else {
     /* LSE over all keys: max, then the sum of exp(sigma - max). */
     double m = order[0].score;
@@ -260,11 +281,11 @@ static void select_row(void* vctx, int64_t r) {
 
 /* Selects keys per row of scores[n_rows][Nk].  Kept indices, ascending, go to
  * idx[r*Nk ...]; counts[r] is their number; cut[r] the selection cut.
- * mode: 0 TOPK(topk), 1 THRESHOLD(tau), 2 MASS(rho). */
+ * mode: 0 TOPK(topk), 1 THRESHOLD(tau), 2 MASS(rho), 3 LEVEL(tau): exp(score) >= tau. */
 int oracle_select(const double* scores, int64_t n_rows, int64_t Nk, int mode, int64_t topk,
                   double tau, double rho, int64_t* counts, int32_t* idx, double* cut,
                   int nthreads) {
-  if (!scores || !counts || !idx || !cut || mode < 0 || mode > 2) return 1;
+  if (!scores || !counts || !idx || !cut || mode < 0 || mode > 3) return 1;
   select_ctx c = {scores, Nk, mode, topk, tau, rho, counts, idx, cut};
   return parallel_for(n_rows, nthreads, select_row, &c);
 }
@@ -343,4 +364,125 @@ int oracle_forward(const uint16_t* q, const uint16_t* k, const uint16_t* v, int6
   if (!q || !k || !v || !row_ptr || !units || !o || !lse || M <= 0 || d <= 0) return 1;
   fwd_ctx c = {{B, H, Nq, Nk, d, M}, q, k, v, scale, row_ptr, col_idx, units, o, lse};
   return parallel_for(n_units, nthreads, forward_unit, &c);
+}
+
+/* ------------------------------------------------------------ dense-step statistics */
+typedef struct {
+  shape_t s;
+  const uint16_t *q, *k;
+  const double* lse;
+  double scale;
+  int stat;
+  const int64_t* units;
+  double* out;
+} colstat_ctx;
+
+/* For every key j: the maximum (stat 0) or the sum (stat 1) over the group's
+ * query rows i of p_ij = exp(s q_i.k_j - lse_i); out holds its natural log. */
+static void colstat_unit(void* vctx, int64_t i) {
+  colstat_ctx* c = (colstat_ctx*)vctx;
+  const shape_t* s = &c->s;
+  const int64_t d = s->d;
+  int64_t u = c->units[i];
+  int64_t bh, g;
+  split_unit(s, u, &bh, &g);
+  int64_t r0 = g * s->M;
+  int64_t r1 = r0 + s->M < s->Nq ? r0 + s->M : s->Nq;
+  double* dst = c->out + i * s->Nk;
+  double* qrows = (double*)malloc(sizeof(double) * (size_t)((r1 - r0) * d));
+  for (int64_t r = r0; r < r1; ++r)
+    for (int64_t e = 0; e < d; ++e) qrows[(r - r0) * d + e] = bf16_value(c->q[(bh * s->Nq + r) * d + e]);
+  for (int64_t j = 0; j < s->Nk; ++j) {
+    const uint16_t* krow = c->k + (bh * s->Nk + j) * d;
+    double stat = 0.0;
+    for (int64_t r = r0; r < r1; ++r) {
+      double lse = c->lse[bh * s->Nq + r];
+      if (!isfinite(lse)) continue;
+      double dot = 0.0;
+      for (int64_t e = 0; e < d; ++e) dot += qrows[(r - r0) * d + e] * bf16_value(krow[e]);
+      double p = exp(c->scale * dot - lse);
+      if (c->stat == ORACLE_STAT_MAX) {
+        if (p > stat) stat = p;
+      } else {
+        stat += p;
+      }
+    }
+    dst[j] = log(stat);
+  }
+  free(qrows);
+}
+
+/* Column statistics of the listed units: out[i*Nk + j] = ln stat_j.
+ * lse: double [B, H, Nq], natural-log row log-sum-exp of the dense step. */
+int oracle_column_stats(const uint16_t* q, const uint16_t* k, const double* lse, int64_t B,
+                        int64_t H, int64_t Nq, int64_t Nk, int64_t d, int64_t M, double scale,
+                        int stat, const int64_t* units, int64_t n_units, double* out,
+                        int nthreads) {
+  if (!q || !k || !lse || !units || !out || M <= 0 || d <= 0 || Nk < 0) return 1;
+  if (stat != ORACLE_STAT_MAX && stat != ORACLE_STAT_SUM) return 1;
+  colstat_ctx c = {{B, H, Nq, Nk, d, M}, q, k, lse, scale, stat, units, out};
+  return parallel_for(n_units, nthreads, colstat_unit, &c);
+}
+
+/* ------------------------------------------------------------ sparse delta */
+typedef struct {
+  shape_t s;
+  const uint16_t *q, *k, *v;
+  double scale;
+  const int64_t* row_ptr;
+  const int32_t* col_idx;
+  const double* lse;
+  const double* base;
+  double sign;
+  const int64_t* units;
+  double* o;
+} delta_ctx;
+
+/* o_i = base_i + sign * sum_{j in list} exp(s q_i.k_j - lse_i) v_j for the
+ * rows of one unit (rows past Nq are zero; a row whose lse is not finite
+ * keeps base_i). */
+static void delta_unit(void* vctx, int64_t i) {
+  delta_ctx* c = (delta_ctx*)vctx;
+  const shape_t* s = &c->s;
+  const int64_t d = s->d, M = s->M;
+  int64_t u = c->units[i];
+  int64_t bh, g;
+  split_unit(s, u, &bh, &g);
+  int64_t begin = c->row_ptr[u], end = c->row_ptr[u + 1];
+  int64_t n = end > begin ? end - begin : 0;
+  const int32_t* list = c->col_idx + begin;
+  double* qrow = (double*)malloc(sizeof(double) * (size_t)d);
+  for (int64_t r = 0; r < M; ++r) {
+    int64_t qi = g * M + r;
+    double* orow = c->o + (i * M + r) * d;
+    for (int64_t e = 0; e < d; ++e) orow[e] = 0.0;
+    if (qi >= s->Nq) continue;
+    if (c->base)
+      for (int64_t e = 0; e < d; ++e) orow[e] = c->base[(bh * s->Nq + qi) * d + e];
+    double lse = c->lse[bh * s->Nq + qi];
+    if (!isfinite(lse)) continue;
+    const uint16_t* qsrc = c->q + (bh * s->Nq + qi) * d;
+    for (int64_t e = 0; e < d; ++e) qrow[e] = bf16_value(qsrc[e]);
+    for (int64_t j = 0; j < n; ++j) {
+      const uint16_t* krow = c->k + (bh * s->Nk + list[j]) * d;
+      double dot = 0.0;
+      for (int64_t e = 0; e < d; ++e) dot += qrow[e] * bf16_value(krow[e]);
+      double p = exp(c->scale * dot - lse);
+      const uint16_t* vrow = c->v + (bh * s->Nk + list[j]) * d;
+      for (int64_t e = 0; e < d; ++e) orow[e] += c->sign * p * bf16_value(vrow[e]);
+    }
+  }
+  free(qrow);
+}
+
+/* Sparse-delta attention of the listed units: o[i][r][e] for r < M.
+ * lse: double [B, H, Nq]; base: double [B, H, Nq, d] or NULL (zero). */
+int oracle_forward_delta(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t B,
+                         int64_t H, int64_t Nq, int64_t Nk, int64_t d, int64_t M, double scale,
+                         const int64_t* row_ptr, const int32_t* col_idx, const double* lse,
+                         const double* base, double sign, const int64_t* units, int64_t n_units,
+                         double* o, int nthreads) {
+  if (!q || !k || !v || !row_ptr || !col_idx || !lse || !units || !o || M <= 0 || d <= 0) return 1;
+  delta_ctx c = {{B, H, Nq, Nk, d, M}, q, k, v, scale, row_ptr, col_idx, lse, base, sign, units, o};
+  return parallel_for(n_units, nthreads, delta_unit, &c);
 }

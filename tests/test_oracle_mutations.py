@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 from tests import test_oracle as pins
+from tests import test_oracle_dense as dpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -20,8 +21,22 @@ MUTATIONS = {
     "forward drops the scale": ("logits[j] = c->scale * dot;", "logits[j] = dot;"),
     "forward exp sign flipped": ("double p = exp(logits[j] - m);", "double p = exp(m - logits[j]);"),
     "lse drops the max": ("lse_unit[r] = m + log(sum);", "lse_unit[r] = log(sum);"),
-    "key row ignores the list": ("c->k + (bh * s->Nk + list[j]) * d", "c->k + (bh * s->Nk + j) * d"),
-    "value row ignores the list": ("c->v + (bh * s->Nk + list[j]) * d", "c->v + (bh * s->Nk + j) * d"),
+    "key row ignores the list": ("c->k + (bh * s->Nk + list[j]) * d;\n      double dot = 0.0;\n"
+                                 "      for (int64_t e = 0; e < d; ++e) dot += qrow[e] * bf16_value(krow[e]);\n"
+                                 "      logits[j]",
+                                 "c->k + (bh * s->Nk + j) * d;\n      double dot = 0.0;\n"
+                                 "      for (int64_t e = 0; e < d; ++e) dot += qrow[e] * bf16_value(krow[e]);\n"
+                                 "      logits[j]"),
+    "delta key row ignores the list": ("c->k + (bh * s->Nk + list[j]) * d;\n      double dot = 0.0;\n"
+                                       "      for (int64_t e = 0; e < d; ++e) dot += qrow[e] * bf16_value(krow[e]);\n"
+                                       "      double p = exp(c->scale * dot - lse);",
+                                       "c->k + (bh * s->Nk + j) * d;\n      double dot = 0.0;\n"
+                                       "      for (int64_t e = 0; e < d; ++e) dot += qrow[e] * bf16_value(krow[e]);\n"
+                                       "      double p = exp(c->scale * dot - lse);"),
+    "value row ignores the list": ("c->v + (bh * s->Nk + list[j]) * d;\n      for (int64_t e = 0; e < d; ++e) orow[e] += p",
+                                   "c->v + (bh * s->Nk + j) * d;\n      for (int64_t e = 0; e < d; ++e) orow[e] += p"),
+    "delta value row ignores the list": ("c->v + (bh * s->Nk + list[j]) * d;\n      for (int64_t e = 0; e < d; ++e) orow[e] += c->sign",
+                                         "c->v + (bh * s->Nk + j) * d;\n      for (int64_t e = 0; e < d; ++e) orow[e] += c->sign"),
     "output not normalised": ("for (int64_t e = 0; e < d; ++e) orow[e] /= sum;", ""),
     "mean divides by M": ("double n = (double)(r1 - r0);", "double n = (double)s->M;"),
     "score drops the scale": ("dst[j] = c->scale * dot;", "dst[j] = dot;"),
@@ -33,7 +48,22 @@ MUTATIONS = {
     "mass stops one late": ("++n;\n        if (acc >= c->rho) break;",
                             "if (acc >= c->rho) break;\n        ++n;"),
     "select lse drops the max": ("double lse = m + log(z);", "double lse = log(z);"),
-    "query row offset wrong": ("c->q + (bh * s->Nq + qi) * d", "c->q + (bh * s->Nq + r) * d"),
+    "query row offset wrong": ("c->q + (bh * s->Nq + qi) * d;\n    for (int64_t e = 0; e < d; ++e) qrow[e] = bf16_value(qsrc[e]);\n    double m",
+                               "c->q + (bh * s->Nq + r) * d;\n    for (int64_t e = 0; e < d; ++e) qrow[e] = bf16_value(qsrc[e]);\n    double m"),
+    "delta query row offset wrong": ("c->q + (bh * s->Nq + qi) * d;\n    for (int64_t e = 0; e < d; ++e) qrow[e] = bf16_value(qsrc[e]);\n    for",
+                                     "c->q + (bh * s->Nq + r) * d;\n    for (int64_t e = 0; e < d; ++e) qrow[e] = bf16_value(qsrc[e]);\n    for"),
+    "column stat drops the lse": ("double p = exp(c->scale * dot - lse);\n      if (c->stat",
+                                  "double p = exp(c->scale * dot);\n      if (c->stat"),
+    "column max keeps the minimum": ("if (p > stat) stat = p;", "if (p < stat || stat == 0.0) stat = p;"),
+    "column stat reads the wrong key": ("c->k + (bh * s->Nk + j) * d;", "c->k + (bh * s->Nk + (j + 1) % s->Nk) * d;"),
+    "column stat lse row offset": ("double lse = c->lse[bh * s->Nq + r];",
+                                   "double lse = c->lse[bh * s->Nq + r - r0];"),
+    "level compares the log": ("exp(order[n].score) >= c->tau", "order[n].score >= c->tau"),
+    "delta ignores the sign": ("orow[e] += c->sign * p * bf16_value(vrow[e]);",
+                               "orow[e] += p * bf16_value(vrow[e]);"),
+    "delta drops the base": ("orow[e] = c->base[(bh * s->Nq + qi) * d + e];", "orow[e] = 0.0;"),
+    "delta drops the lse": ("double p = exp(c->scale * dot - lse);\n      const uint16_t* vrow",
+                            "double p = exp(c->scale * dot);\n      const uint16_t* vrow"),
 }
 
 PINS = [
@@ -45,6 +75,12 @@ PINS = [
     lambda m: pins.test_select_matches_bruteforce_sort(m, "mass", {"rho": 0.9}),
     lambda m: pins.test_select_matches_bruteforce_sort(m, "threshold", {"tau": 0.02}),
     lambda m: pins.test_select_matches_bruteforce_sort(m, "topk", {"topk": 7}),
+    lambda m: dpins.test_column_stats_match_bruteforce(m, "max", (1, 2, 100, 70, 16, 32)),
+    lambda m: dpins.test_column_stats_match_bruteforce(m, "sum", (1, 2, 100, 70, 16, 32)),
+    lambda m: dpins.test_identical_keys_level(m),
+    lambda m: dpins.test_one_hot_keys_keep_own_key(m),
+    lambda m: dpins.test_delta_is_masked_full_softmax(m),
+    lambda m: dpins.test_delta_cache_roundtrip_and_empty(m),
 ]
 
 
