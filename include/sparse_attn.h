@@ -18,6 +18,12 @@
  *  - DiT page (woonyee.org), "Self Attention" and "Online Softmax":
  *    O = softmax(Q K^T / sqrt(d)) V per head, computed tile by tile with a
  *    running max, running sum and running output.
+ *  - FG-Attn review, cached mask (free parameters; Fig. 10): at a dense step
+ *    a slice is kept when one of its full-attention scores reaches
+ *    tau_cached = 0.5/N, and the mask is reused by later steps.  Chipmunk
+ *    review, major comment 2 / Alg. 4: top-k columns by the column sums of
+ *    the attention probabilities; Eq. 1 with Appendix B.2: the sparse delta
+ *    reuses the normalisation constants of an earlier step.
  *
  * Conventions shared by every entry point
  *  - Tensors are row-major [B, H, N, d] with d contiguous (BHND), bf16.
@@ -70,6 +76,10 @@ typedef enum {
   SA_SELECT_THRESHOLD = 1,  /* keep keys whose mean-query probability >= threshold */
   SA_SELECT_MASS = 2        /* keep the fewest top keys whose probability sum >= mass */
 } sa_select_mode;
+
+/* Column statistic of the dense-step builder (sparse_attn_build_index_dense). */
+#define SA_COLSTAT_MAX 0  /* max over the group's queries of p_ij (FG-Attn cached mask) */
+#define SA_COLSTAT_SUM 1  /* sum over the group's queries of p_ij (Chipmunk column sums) */
 
 /* Element type of the attention output o. */
 #define SA_OUT_BF16 0
@@ -160,6 +170,40 @@ sa_status sparse_attn_build_index_noalloc(const sa_problem* problem, const sa_se
                                           int64_t* nnz_out_host, sa_stream_t stream);
 
 /*
+ * Key lists from the attention probabilities of a dense step (FG-Attn
+ * review, cached mask; Chipmunk review, Alg. 4 column sums).  For each unit
+ * (b, h, g) and key j < Nk:
+ *   p_ij   = exp(scale * q_i . k_j - lse_i)   for the group's query rows i,
+ *   stat_j = max_i p_ij (SA_COLSTAT_MAX) or sum_i p_ij (SA_COLSTAT_SUM),
+ * where lse_i is the natural-log log-sum-exp of row i over all Nk keys, as
+ * sparse_attn_forward writes it in its dense mode (row_ptr = col_idx = NULL).
+ * Rows whose lse is not finite count for nothing.  Keys are ranked by
+ * (stat descending, index ascending), then
+ *   TOPK:      the first min(topk, Nk) keys;
+ *   THRESHOLD: keys with stat_j >= threshold (the statistic itself; the
+ *              cached mask uses threshold = 0.5 / Nk with SA_COLSTAT_MAX),
+ *              or the top-ranked key if none qualifies; threshold in
+ *              [0, 1] for MAX, [0, group_size] for SUM;
+ *   MASS:      the shortest ranked prefix whose stat sum reaches mass times
+ *              the sum over all keys (LoSA's retained mass, exact at the
+ *              dense step with SA_COLSTAT_SUM).
+ * Lists, workspace (sparse_attn_build_index_workspace_size bytes), capacity
+ * rules, nnz_out_host, synchronisation and errors are those of
+ * sparse_attn_build_index.  Statistics are computed in fp32 from
+ * tensor-core scores (bf16 inputs, fp32 accumulation), so a key whose
+ * statistic lies within rounding of the cut may fall either side.
+ *
+ *  stat          SA_COLSTAT_MAX or SA_COLSTAT_SUM (else SA_ERR_INVALID_ARG)
+ *  lse           device fp32 [B,H,Nq], 4-byte aligned
+ */
+sa_status sparse_attn_build_index_dense(const sa_problem* problem, const sa_select* select,
+                                        int32_t stat, const void* q, const void* k,
+                                        const float* lse, int64_t* row_ptr, int32_t* col_idx,
+                                        int64_t col_capacity, int64_t* nnz_out_host,
+                                        void* workspace, size_t workspace_bytes,
+                                        sa_stream_t stream);
+
+/*
  * Column-sparse attention forward (FG-Attn review, "What carries the
  * argument": gather-load of the listed K/V rows into tensor-core tiles;
  * Chipmunk review, Alg. 3: softmax renormalised over the kept keys).
@@ -175,6 +219,10 @@ sa_status sparse_attn_build_index_noalloc(const sa_problem* problem, const sa_se
  *  row_ptr       device int64 [B*H*G + 1]
  *  col_idx       device int32 [nnz]
  *  nnz           length of col_idx; every row_ptr entry must lie in [0, nnz]
+ *                row_ptr = col_idx = NULL: dense mode, every unit keeps keys
+ *                0 .. Nk-1 and nnz is ignored (the dense step whose lse
+ *                feeds sparse_attn_build_index_dense); only one of the two
+ *                NULL is SA_ERR_INVALID_ARG
  *  o             device [B,H,Nq,d], written: bf16 (the fp32 result rounded to
  *                nearest even) or fp32, per problem->out_dtype
  *  lse           device fp32 [B,H,Nq], written; nullable
@@ -188,6 +236,35 @@ sa_status sparse_attn_forward(const sa_problem* problem, const void* q, const vo
                               const void* v, const int64_t* row_ptr, const int32_t* col_idx,
                               int64_t nnz, void* o, float* lse, int32_t* dev_status,
                               sa_stream_t stream);
+
+/*
+ * Sparse-delta attention (Chipmunk review, "What carries the argument" and
+ * Eq. 1 as its referee reads it; Appendix B.2: the softmax normalisation of
+ * an earlier step is reused).  For each query row i of unit u with kept
+ * keys K_u:
+ *   o_i = base_i + sign * sum_{j in K_u} exp(scale * q_i . k_j - lse_ref_i) v_j
+ * — a masked full softmax with the caller's normaliser, not renormalised
+ * over K_u.  With lse_ref from a dense step (sparse_attn_forward's dense
+ * mode), sign = -1 and base = that step's output (fp32), the call writes the
+ * cache of the keys outside the lists; a later step adds its own kept keys'
+ * terms back with sign = +1 and base = the cache.  With every key kept, the
+ * true lse, base = NULL and sign = 1 it is dense attention.  A row whose
+ * lse_ref is not finite gets base_i (or 0).
+ *
+ *  q, k, v, row_ptr, col_idx, nnz, dev_status   as for sparse_attn_forward
+ *                (row_ptr = col_idx = NULL keeps every key)
+ *  lse_ref       device fp32 [B,H,Nq], natural log, 4-byte aligned
+ *  base          device fp32 [B,H,Nq,d], 16-byte aligned; NULL = zeros
+ *  sign          finite multiplier of the sum (normally +1 or -1)
+ *  o             device [B,H,Nq,d] in problem->out_dtype; may be base itself
+ *                when the output is fp32 (in place), must not overlap it
+ *                otherwise
+ */
+sa_status sparse_attn_forward_delta(const sa_problem* problem, const void* q, const void* k,
+                                    const void* v, const int64_t* row_ptr,
+                                    const int32_t* col_idx, int64_t nnz, const float* lse_ref,
+                                    const float* base, float sign, void* o, int32_t* dev_status,
+                                    sa_stream_t stream);
 
 /*
  * Checks index lists without trapping: row_ptr[0] == 0, row_ptr[rows] == nnz,

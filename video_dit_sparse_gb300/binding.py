@@ -21,6 +21,8 @@ SA_ERR_BAD_INDEX, SA_ERR_TIMEOUT, SA_ERR_CUDA = 4, 5, 6
 SA_DEVERR_ROW_PTR, SA_DEVERR_INDEX, SA_DEVERR_TIMEOUT, SA_DEVERR_CAPACITY = 1, 2, 4, 8
 SA_SELECT_TOPK, SA_SELECT_THRESHOLD, SA_SELECT_MASS = 0, 1, 2
 _MODES = {"topk": SA_SELECT_TOPK, "threshold": SA_SELECT_THRESHOLD, "mass": SA_SELECT_MASS}
+SA_COLSTAT_MAX, SA_COLSTAT_SUM = 0, 1
+_STATS = {"max": SA_COLSTAT_MAX, "sum": SA_COLSTAT_SUM}
 
 
 class SparseAttnError(RuntimeError):
@@ -56,8 +58,15 @@ def _load():
     lib.sparse_attn_build_index.argtypes = [P(sa_problem), P(sa_select), vp, vp, vp, vp, i64,
                                             P(ctypes.c_int64), vp, ctypes.c_size_t, vp]
     lib.sparse_attn_build_index.restype = ctypes.c_int
+    lib.sparse_attn_build_index_dense.argtypes = [P(sa_problem), P(sa_select), ctypes.c_int32, vp,
+                                                  vp, vp, vp, vp, i64, P(ctypes.c_int64), vp,
+                                                  ctypes.c_size_t, vp]
+    lib.sparse_attn_build_index_dense.restype = ctypes.c_int
     lib.sparse_attn_forward.argtypes = [P(sa_problem), vp, vp, vp, vp, vp, i64, vp, vp, vp, vp]
     lib.sparse_attn_forward.restype = ctypes.c_int
+    lib.sparse_attn_forward_delta.argtypes = [P(sa_problem), vp, vp, vp, vp, vp, i64, vp, vp,
+                                              ctypes.c_float, vp, vp, vp]
+    lib.sparse_attn_forward_delta.restype = ctypes.c_int
     lib.sparse_attn_validate_index.argtypes = [P(sa_problem), vp, vp, i64, vp, vp]
     lib.sparse_attn_validate_index.restype = ctypes.c_int
     lib.sparse_attn_status_string.argtypes = [ctypes.c_int]
@@ -111,19 +120,8 @@ def sparse_attn_build_index_workspace_size(p: sa_problem) -> int:
     return int(lib.sparse_attn_build_index_workspace_size(ctypes.byref(p)))
 
 
-def sparse_attn_build_index(q: torch.Tensor, k: torch.Tensor, mode="topk", *, topk: int = 0,
-                            threshold: float = 0.0, mass: float = 0.99, group_size: int = 128,
-                            scale: float | None = None, col_capacity: int | None = None,
-                            workspace: torch.Tensor | None = None, stream=None,
-                            sync_nnz: bool | None = None):
-    """Builds CSR key lists; returns (row_ptr int64, col_idx int32, nnz).
-
-    By default the call synchronises and raises on any device-side error
-    (capacity, timeout).  ``sync_nnz=False`` keeps a TOPK call fully
-    asynchronous (nnz is then known up front).  For THRESHOLD/MASS col_idx is
-    allocated for the worst case (every key) unless col_capacity is given;
-    col_idx is returned trimmed to nnz (a view).
-    """
+def _build(q, k, mode, topk, threshold, mass, group_size, scale, col_capacity, workspace,
+           stream, sync_nnz, stat=None, lse=None):
     _check(q, torch.bfloat16, "q")
     _check(k, torch.bfloat16, "k")
     p = problem(q, k, group_size, scale)
@@ -142,27 +140,69 @@ def sparse_attn_build_index(q: torch.Tensor, k: torch.Tensor, mode="topk", *, to
     if sync_nnz is None:
         sync_nnz = True
     nnz = ctypes.c_int64(0)
-    st = lib.sparse_attn_build_index(ctypes.byref(p), ctypes.byref(sel), _ptr(q), _ptr(k),
-                                     _ptr(row_ptr), _ptr(col_idx), int(col_capacity),
-                                     ctypes.byref(nnz) if sync_nnz else None, _ptr(workspace),
-                                     workspace.numel(), _stream(stream))
+    nnz_ref = ctypes.byref(nnz) if sync_nnz else None
+    if stat is None:
+        st = lib.sparse_attn_build_index(ctypes.byref(p), ctypes.byref(sel), _ptr(q), _ptr(k),
+                                         _ptr(row_ptr), _ptr(col_idx), int(col_capacity), nnz_ref,
+                                         _ptr(workspace), workspace.numel(), _stream(stream))
+        where = "sparse_attn_build_index"
+    else:
+        _check(lse, torch.float32, "lse")
+        st = lib.sparse_attn_build_index_dense(ctypes.byref(p), ctypes.byref(sel),
+                                               _STATS.get(stat, stat), _ptr(q), _ptr(k), _ptr(lse),
+                                               _ptr(row_ptr), _ptr(col_idx), int(col_capacity),
+                                               nnz_ref, _ptr(workspace), workspace.numel(),
+                                               _stream(stream))
+        where = "sparse_attn_build_index_dense"
     if st != SA_OK:
-        raise SparseAttnError(st, "sparse_attn_build_index")
+        raise SparseAttnError(st, where)
     n = nnz.value if sync_nnz else rows * min(max(int(topk), 1), p.Nk)
     return row_ptr, col_idx[:n], n
 
 
-def sparse_attn_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_ptr: torch.Tensor,
-                        col_idx: torch.Tensor, *, group_size: int = 128, scale: float | None = None,
-                        nnz: int | None = None, out: torch.Tensor | None = None,
-                        out_dtype=torch.bfloat16, lse: torch.Tensor | bool = True,
-                        status: torch.Tensor | None = None, stream=None):
-    """Column-sparse attention; returns (o [B,H,Nq,d] in out_dtype (bf16 or
-    fp32; taken from `out` if given), lse fp32 [B,H,Nq] or None)."""
+def sparse_attn_build_index(q: torch.Tensor, k: torch.Tensor, mode="topk", *, topk: int = 0,
+                            threshold: float = 0.0, mass: float = 0.99, group_size: int = 128,
+                            scale: float | None = None, col_capacity: int | None = None,
+                            workspace: torch.Tensor | None = None, stream=None,
+                            sync_nnz: bool | None = None):
+    """Builds CSR key lists from mean-query scores; returns (row_ptr int64,
+    col_idx int32, nnz).
+
+    By default the call synchronises and raises on any device-side error
+    (capacity, timeout).  ``sync_nnz=False`` keeps a TOPK call fully
+    asynchronous (nnz is then known up front).  For THRESHOLD/MASS col_idx is
+    allocated for the worst case (every key) unless col_capacity is given;
+    col_idx is returned trimmed to nnz (a view).
+    """
+    return _build(q, k, mode, topk, threshold, mass, group_size, scale, col_capacity, workspace,
+                  stream, sync_nnz)
+
+
+def sparse_attn_build_index_dense(q: torch.Tensor, k: torch.Tensor, lse: torch.Tensor,
+                                  stat="max", mode="threshold", *, topk: int = 0,
+                                  threshold: float = 0.0, mass: float = 0.99,
+                                  group_size: int = 128, scale: float | None = None,
+                                  col_capacity: int | None = None,
+                                  workspace: torch.Tensor | None = None, stream=None,
+                                  sync_nnz: bool | None = None):
+    """Key lists from a dense step's attention probabilities (column max or
+    column sum over each group of exp(scale q.k - lse)); `lse` fp32
+    [B,H,Nq] as the dense forward writes it.  THRESHOLD compares the
+    statistic itself with `threshold` (the cached mask: stat "max",
+    threshold 0.5/Nk).  Returns (row_ptr, col_idx, nnz) like
+    sparse_attn_build_index."""
+    return _build(q, k, mode, topk, threshold, mass, group_size, scale, col_capacity, workspace,
+                  stream, sync_nnz, stat=stat, lse=lse)
+
+
+def _fwd_common(q, k, v, row_ptr, col_idx, group_size, scale, nnz, out, out_dtype):
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check(t, torch.bfloat16, n)
-    _check(row_ptr, torch.int64, "row_ptr")
-    _check(col_idx, torch.int32, "col_idx")
+    if (row_ptr is None) != (col_idx is None):
+        raise ValueError("row_ptr and col_idx are both given or both None (dense)")
+    if row_ptr is not None:
+        _check(row_ptr, torch.int64, "row_ptr")
+        _check(col_idx, torch.int32, "col_idx")
     if v.shape != k.shape:
         raise ValueError("v must have k's shape")
     if out is not None:
@@ -171,18 +211,56 @@ def sparse_attn_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, row_p
     p = problem(q, k, group_size, scale, out_dtype)
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if row_ptr is None:
+        return p, out, None, None, 0
+    if nnz is None:
+        nnz = col_idx.numel()
+    return p, out, _ptr(row_ptr), (_ptr(col_idx) if col_idx.numel() else None), int(nnz)
+
+
+def sparse_attn_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                        row_ptr: torch.Tensor | None, col_idx: torch.Tensor | None, *,
+                        group_size: int = 128, scale: float | None = None,
+                        nnz: int | None = None, out: torch.Tensor | None = None,
+                        out_dtype=torch.bfloat16, lse: torch.Tensor | bool = True,
+                        status: torch.Tensor | None = None, stream=None):
+    """Column-sparse attention; returns (o [B,H,Nq,d] in out_dtype (bf16 or
+    fp32; taken from `out` if given), lse fp32 [B,H,Nq] or None).
+    row_ptr = col_idx = None: dense attention (every key kept)."""
+    p, out, rp, ci, nnz = _fwd_common(q, k, v, row_ptr, col_idx, group_size, scale, nnz, out,
+                                      out_dtype)
     if lse is True:
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     elif lse is False:
         lse = None
-    if nnz is None:
-        nnz = col_idx.numel()
-    st = lib.sparse_attn_forward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr),
-                                 _ptr(col_idx) if col_idx.numel() else None, int(nnz), _ptr(out),
-                                 _ptr(lse), _ptr(status), _stream(stream))
+    st = lib.sparse_attn_forward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), rp, ci, nnz,
+                                 _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
     if st != SA_OK:
         raise SparseAttnError(st, "sparse_attn_forward")
     return out, lse
+
+
+def sparse_attn_forward_delta(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                              row_ptr: torch.Tensor | None, col_idx: torch.Tensor | None,
+                              lse_ref: torch.Tensor, *, base: torch.Tensor | None = None,
+                              sign: float = 1.0, group_size: int = 128,
+                              scale: float | None = None, nnz: int | None = None,
+                              out: torch.Tensor | None = None, out_dtype=torch.float32,
+                              status: torch.Tensor | None = None, stream=None):
+    """Sparse delta: o = base + sign * sum over kept j of
+    exp(scale q.k_j - lse_ref) v_j (fp32 base, fp32 output by default;
+    out=base updates the cache in place)."""
+    _check(lse_ref, torch.float32, "lse_ref")
+    if base is not None:
+        _check(base, torch.float32, "base")
+    p, out, rp, ci, nnz = _fwd_common(q, k, v, row_ptr, col_idx, group_size, scale, nnz, out,
+                                      out_dtype)
+    st = lib.sparse_attn_forward_delta(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), rp, ci, nnz,
+                                       _ptr(lse_ref), _ptr(base), float(sign), _ptr(out),
+                                       _ptr(status), _stream(stream))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_forward_delta")
+    return out
 
 
 def sparse_attn_validate_index(row_ptr: torch.Tensor, col_idx: torch.Tensor, *, B: int, H: int,
@@ -204,5 +282,7 @@ def sparse_attn_validate_index(row_ptr: torch.Tensor, col_idx: torch.Tensor, *, 
 
 # Short aliases for Python callers.
 build_index = sparse_attn_build_index
+build_index_dense = sparse_attn_build_index_dense
 forward = sparse_attn_forward
+forward_delta = sparse_attn_forward_delta
 validate_index = sparse_attn_validate_index

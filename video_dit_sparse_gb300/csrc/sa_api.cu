@@ -114,19 +114,31 @@ size_t sparse_attn_build_index_workspace_size(const sa_problem* p) {
   return sa::build_layout(dims.rows, p->Nk, p->d).total;
 }
 
-sa_status sparse_attn_build_index(const sa_problem* p, const sa_select* sel, const void* q,
-                                  const void* k, int64_t* row_ptr, int32_t* col_idx,
-                                  int64_t col_capacity, int64_t* nnz_out_host, void* workspace,
-                                  size_t workspace_bytes, sa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by the mean-query and the dense-step builders: stat < 0 selects
+// the mean-query scores, otherwise the column statistic of p_ij =
+// exp(scale q_i.k_j - lse_i) (0 max, 1 sum) with `lse` [B,H,Nq].
+sa_status build_common(const sa_problem* p, const sa_select* sel, int32_t stat, const void* q,
+                       const void* k, const float* lse, int64_t* row_ptr, int32_t* col_idx,
+                       int64_t col_capacity, int64_t* nnz_out_host, void* workspace,
+                       size_t workspace_bytes, sa_stream_t stream) {
   Dims dims;
   sa_status st = check_problem(p, &dims);
   if (st != SA_OK) return st;
   if (!sel || sel->mode < SA_SELECT_TOPK || sel->mode > SA_SELECT_MASS) return SA_ERR_INVALID_ARG;
   if (sel->mode == SA_SELECT_TOPK && sel->topk < 1) return SA_ERR_INVALID_ARG;
-  if (sel->mode == SA_SELECT_THRESHOLD && !(sel->threshold >= 0.0 && sel->threshold <= 1.0))
-    return SA_ERR_INVALID_ARG;
+  if (sel->mode == SA_SELECT_THRESHOLD) {
+    // a probability for the mean-query rule and the column maximum; a column
+    // sum can reach the group's row count
+    const double tmax = stat == 1 ? double(p->group_size) : 1.0;
+    if (!(sel->threshold >= 0.0 && sel->threshold <= tmax)) return SA_ERR_INVALID_ARG;
+  }
   if (sel->mode == SA_SELECT_MASS && !(sel->mass > 0.0 && sel->mass <= 1.0)) return SA_ERR_INVALID_ARG;
   if (!q || !k || !row_ptr || !workspace || col_capacity < 0) return SA_ERR_INVALID_ARG;
+  if (stat >= 0 && (!lse || !aligned(lse, 4))) return SA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(row_ptr, 8) || !aligned(workspace, 256) ||
       (col_idx && !aligned(col_idx, 4)))
     return SA_ERR_INVALID_ARG;
@@ -150,12 +162,15 @@ sa_status sparse_attn_build_index(const sa_problem* p, const sa_select* sel, con
   if (!in_device_allocation(q, qbytes) || !in_device_allocation(k, kbytes) ||
       !in_device_allocation(row_ptr, uint64_t(dims.rows + 1) * 8) ||
       !in_device_allocation(workspace, L.total) ||
+      (stat >= 0 && !in_device_allocation(lse, uint64_t(p->B) * p->H * p->Nq * 4)) ||
       (col_capacity > 0 && !in_device_allocation(col_idx, uint64_t(col_capacity) * 4)))
     return SA_ERR_INVALID_ARG;
 
   sa::BuildArgs a;
   a.q = static_cast<const uint16_t*>(q);
   a.k = static_cast<const uint16_t*>(k);
+  a.lse = lse;
+  a.stat = stat;
   a.row_ptr = row_ptr;
   a.col_idx = col_idx;
   a.col_capacity = col_capacity;
@@ -188,48 +203,112 @@ sa_status sparse_attn_build_index(const sa_problem* p, const sa_select* sel, con
   return SA_OK;
 }
 
-sa_status sparse_attn_forward(const sa_problem* p, const void* q, const void* k, const void* v,
-                              const int64_t* row_ptr, const int32_t* col_idx, int64_t nnz,
-                              void* o, float* lse, int32_t* dev_status, sa_stream_t stream) {
+// Argument checks and FwdArgs shared by the forward and the sparse delta.
+// row_ptr == col_idx == NULL: every unit keeps all keys (nnz ignored).
+sa_status forward_args(const sa_problem* p, const void* q, const void* k, const void* v,
+                       const int64_t* row_ptr, const int32_t* col_idx, int64_t nnz, void* o,
+                       float* lse, int32_t* dev_status, sa::FwdArgs* a, int* sms) {
   Dims dims;
   sa_status st = check_problem(p, &dims);
   if (st != SA_OK) return st;
-  if (!q || !k || !v || !row_ptr || !o || nnz < 0 || (nnz > 0 && !col_idx)) return SA_ERR_INVALID_ARG;
+  const bool dense = !row_ptr && !col_idx;
+  if (!q || !k || !v || !o || (!dense && (!row_ptr || nnz < 0 || (nnz > 0 && !col_idx))))
+    return SA_ERR_INVALID_ARG;
+  if (dense) nnz = 0;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
-      !aligned(row_ptr, 8) || (col_idx && !aligned(col_idx, 4)) || (lse && !aligned(lse, 4)) ||
+      (row_ptr && !aligned(row_ptr, 8)) || (col_idx && !aligned(col_idx, 4)) || (lse && !aligned(lse, 4)) ||
       (dev_status && !aligned(dev_status, 4)))
     return SA_ERR_INVALID_ARG;
-  int sms = 0;
-  if ((st = device_info(&sms)) != SA_OK) return st;
+  if ((st = device_info(sms)) != SA_OK) return st;
   const uint64_t qbytes = uint64_t(p->B) * p->H * p->Nq * p->d * 2;
   const uint64_t kbytes = uint64_t(p->B) * p->H * p->Nk * p->d * 2;
   const uint64_t obytes = p->out_dtype == SA_OUT_FP32 ? 2 * qbytes : qbytes;
   if (!in_device_allocation(q, qbytes) || !in_device_allocation(k, kbytes) ||
       !in_device_allocation(v, kbytes) || !in_device_allocation(o, obytes) ||
-      !in_device_allocation(row_ptr, uint64_t(dims.rows + 1) * 8) ||
+      (!dense && !in_device_allocation(row_ptr, uint64_t(dims.rows + 1) * 8)) ||
       (nnz > 0 && !in_device_allocation(col_idx, uint64_t(nnz) * 4)) ||
       (lse && !in_device_allocation(lse, uint64_t(p->B) * p->H * p->Nq * 4)) ||
       (dev_status && !in_device_allocation(dev_status, 4)))
     return SA_ERR_INVALID_ARG;
+  a->q = static_cast<const uint16_t*>(q);
+  a->k = static_cast<const uint16_t*>(k);
+  a->v = static_cast<const uint16_t*>(v);
+  a->row_ptr = row_ptr;
+  a->col_idx = col_idx;
+  a->nnz = nnz;
+  a->dense = dense ? 1 : 0;
+  a->o = o;
+  a->out_fp32 = p->out_dtype == SA_OUT_FP32 ? 1 : 0;
+  a->lse = lse;
+  a->status = dev_status;
+  a->units = dims.rows;
+  a->G = dims.G;
+  a->Nq = p->Nq;
+  a->Nk = p->Nk;
+  a->M = p->group_size;
+  a->neg_scale = p->scale < 0.f ? 1 : 0;
+  a->scale_log2 = static_cast<float>(std::fabs(static_cast<double>(p->scale)) * 1.4426950408889634);
+  return SA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sa_status sparse_attn_build_index(const sa_problem* p, const sa_select* sel, const void* q,
+                                  const void* k, int64_t* row_ptr, int32_t* col_idx,
+                                  int64_t col_capacity, int64_t* nnz_out_host, void* workspace,
+                                  size_t workspace_bytes, sa_stream_t stream) {
+  return build_common(p, sel, -1, q, k, nullptr, row_ptr, col_idx, col_capacity, nnz_out_host,
+                      workspace, workspace_bytes, stream);
+}
+
+sa_status sparse_attn_build_index_dense(const sa_problem* p, const sa_select* sel, int32_t stat,
+                                        const void* q, const void* k, const float* lse,
+                                        int64_t* row_ptr, int32_t* col_idx, int64_t col_capacity,
+                                        int64_t* nnz_out_host, void* workspace,
+                                        size_t workspace_bytes, sa_stream_t stream) {
+  if (stat != SA_COLSTAT_MAX && stat != SA_COLSTAT_SUM) return SA_ERR_INVALID_ARG;
+  return build_common(p, sel, stat, q, k, lse, row_ptr, col_idx, col_capacity, nnz_out_host,
+                      workspace, workspace_bytes, stream);
+}
+
+sa_status sparse_attn_forward(const sa_problem* p, const void* q, const void* k, const void* v,
+                              const int64_t* row_ptr, const int32_t* col_idx, int64_t nnz,
+                              void* o, float* lse, int32_t* dev_status, sa_stream_t stream) {
   sa::FwdArgs a;
-  a.q = static_cast<const uint16_t*>(q);
-  a.k = static_cast<const uint16_t*>(k);
-  a.v = static_cast<const uint16_t*>(v);
-  a.row_ptr = row_ptr;
-  a.col_idx = col_idx;
-  a.nnz = nnz;
-  a.o = o;
-  a.out_fp32 = p->out_dtype == SA_OUT_FP32 ? 1 : 0;
-  a.lse = lse;
-  a.status = dev_status;
-  a.units = dims.rows;
-  a.G = dims.G;
-  a.Nq = p->Nq;
-  a.Nk = p->Nk;
-  a.M = p->group_size;
-  a.neg_scale = p->scale < 0.f ? 1 : 0;
-  a.scale_log2 = static_cast<float>(std::fabs(static_cast<double>(p->scale)) * 1.4426950408889634);
+  int sms = 0;
+  sa_status st = forward_args(p, q, k, v, row_ptr, col_idx, nnz, o, lse, dev_status, &a, &sms);
+  if (st != SA_OK) return st;
   return map_cuda(sa::launch_forward(a, p->d, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sa_status sparse_attn_forward_delta(const sa_problem* p, const void* q, const void* k,
+                                    const void* v, const int64_t* row_ptr,
+                                    const int32_t* col_idx, int64_t nnz, const float* lse_ref,
+                                    const float* base, float sign, void* o, int32_t* dev_status,
+                                    sa_stream_t stream) {
+  sa::FwdArgs a;
+  int sms = 0;
+  sa_status st = forward_args(p, q, k, v, row_ptr, col_idx, nnz, o, nullptr, dev_status, &a, &sms);
+  if (st != SA_OK) return st;
+  if (!lse_ref || !aligned(lse_ref, 4) || !std::isfinite(sign) || (base && !aligned(base, 16)))
+    return SA_ERR_INVALID_ARG;
+  const uint64_t rows = uint64_t(p->B) * p->H * p->Nq;
+  const uint64_t base_bytes = rows * p->d * 4;
+  const uint64_t obytes = rows * p->d * (p->out_dtype == SA_OUT_FP32 ? 4 : 2);
+  if (!in_device_allocation(lse_ref, rows * 4) || (base && !in_device_allocation(base, base_bytes)))
+    return SA_ERR_INVALID_ARG;
+  if (base && base != o) {
+    // distinct buffers must not overlap (in-place needs o == base, fp32 output)
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(base), o0 = reinterpret_cast<uintptr_t>(o);
+    if (b0 < o0 + obytes && o0 < b0 + base_bytes) return SA_ERR_INVALID_ARG;
+  }
+  if (base && base == o && p->out_dtype != SA_OUT_FP32) return SA_ERR_INVALID_ARG;
+  a.lse_ref = lse_ref;
+  a.base = base;
+  a.sign = sign;
+  return map_cuda(sa::launch_forward_delta(a, p->d, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 sa_status sparse_attn_validate_index(const sa_problem* p, const int64_t* row_ptr,

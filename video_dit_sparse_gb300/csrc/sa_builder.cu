@@ -326,6 +326,7 @@ struct SelArgs {
   int32_t* col_idx;      // TOPK only: lists are emitted by the select kernel
   int64_t col_capacity;
   int32_t mask_words;    // TOPK: words of the kept-key bitmask (0: emit by re-reading the row)
+  int32_t level;         // THRESHOLD compares the score itself with ln(threshold)
 };
 
 constexpr int kSelThreads = 256;            // one row per block, 4 blocks resident per SM
@@ -800,7 +801,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
     float rz = 0.f;
 #pragma unroll
     for (int w = 0; w < kSelWarps; ++w) rz += sm.fred[1][w];
-    const float c = a.log_tau + rmax + logf(rz);
+    // LEVEL (dense-step statistics): the score is already ln of a probability
+    const float c = a.level ? a.log_tau : a.log_tau + rmax + logf(rz);
     const uint32_t kc = (c == -INFINITY) ? 0u : order_key(c);
     int64_t n = 0;
     for_each_key(s, Nk, [&](int, float x) { n += order_key(x) >= kc; });
@@ -1191,20 +1193,29 @@ static cudaError_t launch_scores(const BuildArgs& a, int num_sms, cudaStream_t s
   return cudaGetLastError();
 }
 
+cudaError_t launch_colstat(const BuildArgs& b, float* scores, int32_t* status, int num_sms,
+                           cudaStream_t st);
+
 cudaError_t launch_build_index(const BuildArgs& a, int num_sms, cudaStream_t st) {
   int64_t* misc = reinterpret_cast<int64_t*>(a.ws + a.L.misc);
   int32_t* status = reinterpret_cast<int32_t*>(misc + 1);
   cudaError_t e = cudaMemsetAsync(misc, 0, 16, st);
   if (e != cudaSuccess) return e;
-  uint16_t* qhi = reinterpret_cast<uint16_t*>(a.ws + a.L.qhi);
-  uint16_t* qlo = reinterpret_cast<uint16_t*>(a.ws + a.L.qlo);
-  if (a.d == 128)
-    sa_meanq_kernel<128><<<static_cast<unsigned>(a.rows), 256, 0, st>>>(a.q, qhi, qlo, a.G, a.Nq, a.M);
-  else
-    sa_meanq_kernel<64><<<static_cast<unsigned>(a.rows), 256, 0, st>>>(a.q, qhi, qlo, a.G, a.Nq, a.M);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  e = a.d == 128 ? launch_scores<128>(a, num_sms, st, status) : launch_scores<64>(a, num_sms, st, status);
-  if (e != cudaSuccess) return e;
+  if (a.stat >= 0) {
+    // dense-step statistics of the full attention probabilities
+    e = launch_colstat(a, reinterpret_cast<float*>(a.ws + a.L.scores), status, num_sms, st);
+    if (e != cudaSuccess) return e;
+  } else {
+    uint16_t* qhi = reinterpret_cast<uint16_t*>(a.ws + a.L.qhi);
+    uint16_t* qlo = reinterpret_cast<uint16_t*>(a.ws + a.L.qlo);
+    if (a.d == 128)
+      sa_meanq_kernel<128><<<static_cast<unsigned>(a.rows), 256, 0, st>>>(a.q, qhi, qlo, a.G, a.Nq, a.M);
+    else
+      sa_meanq_kernel<64><<<static_cast<unsigned>(a.rows), 256, 0, st>>>(a.q, qhi, qlo, a.G, a.Nq, a.M);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = a.d == 128 ? launch_scores<128>(a, num_sms, st, status) : launch_scores<64>(a, num_sms, st, status);
+    if (e != cudaSuccess) return e;
+  }
   SelArgs s;
   s.scores = reinterpret_cast<const float*>(a.ws + a.L.scores);
   s.ld = a.L.ld;
@@ -1213,6 +1224,7 @@ cudaError_t launch_build_index(const BuildArgs& a, int num_sms, cudaStream_t st)
   s.topk = a.topk;
   s.log_tau = a.threshold > 0.0 ? static_cast<float>(log(a.threshold)) : -INFINITY;
   s.mass = a.mass;
+  s.level = a.stat >= 0 ? 1 : 0;
   s.cut = reinterpret_cast<uint32_t*>(a.ws + a.L.cut);
   s.ties = reinterpret_cast<int32_t*>(a.ws + a.L.ties);
   s.counts = reinterpret_cast<int64_t*>(a.ws + a.L.counts);

@@ -19,7 +19,17 @@
 //                 the epilogue writes O / l in bf16 and lse = m + ln l.
 // The softmax is restricted to the kept keys (Chipmunk review, major
 // comment 1, Alg. 3).  Groups longer than 128 rows (C = 192) use two
-// 128-row blocks that share every K/V tile.
+// 128-row blocks that share every K/V tile.  Without index lists every unit
+// keeps all keys in order (dense attention, the dense step of a cached
+// mask).
+//
+// The DELTA variant is the Chipmunk review's sparse delta (Eq. 1 with the
+// normalisation constants of an earlier step, Appendix B.2): no running max
+// and no renormalisation; P = exp(l - lse_ref) with the caller's per-row
+// lse_ref, and the epilogue writes base + sign * P V.  Without the final
+// division nothing cancels the rounding of P, so P goes to the PV MMA as two
+// bf16 terms (hi and the rounded remainder, in the two halves of the S
+// buffer) and O accumulates both products.
 #include "sa_device.cuh"
 #include "sa_internal.h"
 #include "sa_tma.h"
@@ -85,6 +95,11 @@ struct FwdBars {
 // Unit u's list bounds.  A malformed row_ptr pair makes the unit empty.
 __device__ __forceinline__ int64_t unit_list(const FwdArgs& a, int64_t u, int64_t* begin,
                                              bool* bad) {
+  if (a.dense) {
+    *bad = false;
+    *begin = 0;
+    return a.Nk;
+  }
   const int64_t b0 = __ldg(a.row_ptr + u), b1 = __ldg(a.row_ptr + u + 1);
   if (b0 < 0 || b1 < b0 || b1 > a.nnz) {
     *bad = true;
@@ -96,7 +111,41 @@ __device__ __forceinline__ int64_t unit_list(const FwdArgs& a, int64_t u, int64_
   return b1 - b0;
 }
 
-template <int D, int RB, int BN, int STAGES>
+// Writes row values o[c] = base[c] + sign * acc[c] * inv for 32 columns
+// starting at column c0 (bf16 RNE or fp32 output).
+__device__ __forceinline__ void store_row32(const FwdArgs& a, int64_t orow_off, int c0,
+                                            const uint32_t* acc, float mul, bool delta) {
+  float v[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(acc[e]) * mul;
+  if (delta && a.base) {
+    const float4* b4 = reinterpret_cast<const float4*>(a.base + orow_off + c0);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float4 b = __ldg(b4 + e);
+      v[4 * e] += b.x;
+      v[4 * e + 1] += b.y;
+      v[4 * e + 2] += b.z;
+      v[4 * e + 3] += b.w;
+    }
+  }
+  if (a.out_fp32) {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(a.o) + orow_off + c0);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      dst[e] = make_uint4(__float_as_uint(v[4 * e]), __float_as_uint(v[4 * e + 1]),
+                          __float_as_uint(v[4 * e + 2]), __float_as_uint(v[4 * e + 3]));
+  } else {
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) w[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + orow_off + c0);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+  }
+}
+
+template <int D, int RB, int BN, int STAGES, bool DELTA>
 __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     sa_forward_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq) {
   using C = FwdCfg<D, RB, BN, STAGES>;
@@ -163,6 +212,14 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
       const int64_t orow_off = (bh * a.Nq + grow) * D;
       const uint32_t n = static_cast<uint32_t>((len + BN - 1) / BN);
       if (n == 0) {
+        if (DELTA) {
+          if (valid) {
+            const uint32_t zero[32] = {};
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) store_row32(a, orow_off, c * 32, zero, 0.f, true);
+          }
+          continue;
+        }
         if (valid) {
           const uint4 z = make_uint4(0, 0, 0, 0);
           uint4* dst = a.out_fp32 ? reinterpret_cast<uint4*>(static_cast<float*>(a.o) + orow_off)
@@ -175,6 +232,11 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
       }
       const float sl = a.scale_log2;  // |scale| * log2(e) > 0
       float m = -INFINITY, l = 0.f, lr = 0.f;
+      if (DELTA) {
+        // the fixed normaliser in exp2 units; a row without a finite one adds nothing
+        const float lr0 = valid ? __ldg(a.lse_ref + bh * a.Nq + grow) : INFINITY;
+        m = isfinite(lr0) ? lr0 * 1.4426950408889634f : INFINITY;
+      }
       for (uint32_t j = 0; j < n; ++j) {
         const uint32_t tt = t + j, b = tt & 1;
         const int nvalid = static_cast<int>(min64(BN, len - int64_t(j) * BN));
@@ -196,8 +258,8 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         }
         // Row max of the raw scores (scale > 0 commutes with max): 3-input
         // maxima in 8 chains.
-        float mx;
-        {
+        float mx = 0.f;
+        if (!DELTA) {
           float t8[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) t8[i] = fmaxf(x[i], x[8 + i]);
@@ -208,7 +270,8 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           mx = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
         }
         mx *= sl;
-        if (j == 0) {
+        if (DELTA) {
+        } else if (j == 0) {
           m = mx;
         } else if (__any_sync(0xffffffffu, mx > m + C::kRescaleLog2)) {
           // O must hold PV of the previous tile before it is rescaled.
@@ -240,6 +303,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         // convex combination of V rows whatever the rounding.
         const uint64_t sl2 = f2(sl, sl), nm2 = f2(-m, -m);
         uint32_t p[BN / 2];
+        uint32_t plo[DELTA ? BN / 2 : 1];
         uint64_t ps[4] = {0, 0, 0, 0};
         float pr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -247,16 +311,24 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           const uint64_t y = fma2(f2(x[2 * c], x[2 * c + 1]), sl2, nm2);
           const float p0 = fast_exp2(f2lo(y)), p1 = fast_exp2(f2hi(y));
           p[c] = pack_bf16(p0, p1);
-          ps[c & 3] = add2(ps[c & 3], f2(p0, p1));
-          pr[c & 3] = add_bf16x2(p[c], pr[c & 3]);
+          if (!DELTA) {
+            ps[c & 3] = add2(ps[c & 3], f2(p0, p1));
+            pr[c & 3] = add_bf16x2(p[c], pr[c & 3]);
+          } else {
+            plo[c] = pack_bf16(p0 - __uint_as_float(p[c] << 16), p1 - __uint_as_float(p[c] & 0xFFFF0000u));
+          }
         }
-        {
+        if (!DELTA) {
           const uint64_t s2 = add2(add2(ps[0], ps[1]), add2(ps[2], ps[3]));
           l += f2lo(s2) + f2hi(s2);
           lr += (pr[0] + pr[1]) + (pr[2] + pr[3]);
         }
 #pragma unroll
         for (int c = 0; c < BN / 64; ++c) tmem_st32(sbase + c * 32, p + c * 32);
+        if (DELTA) {
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c) tmem_st32(sbase + BN / 2 + c * 32, plo + c * 32);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->pfull[b][rb]);
@@ -265,34 +337,16 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         const uint32_t tl = t + n - 1;
         if (!mbar_wait(&bars->pvdone[tl & 1][rb], (tl >> 1) & 1, abort)) goto done;
         tc_fence_after();
-        const float inv = 1.f / lr;
+        const float inv = DELTA ? a.sign : 1.f / lr;
         const uint32_t obase = tmem + lane_base + C::kOCol + rb * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(obase + c * 32, r);
           tmem_ld_wait();
-          if (a.out_fp32) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * inv);
-            if (valid) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(a.o) + orow_off + c * 32);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) dst[e] = make_uint4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
-            }
-          } else {
-            uint32_t w[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              w[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
-            if (valid) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + orow_off + c * 32);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-            }
-          }
+          if (valid) store_row32(a, orow_off, c * 32, r, inv, DELTA);
         }
-        if (valid && a.lse) a.lse[bh * a.Nq + grow] = m * 0.69314718055994531f + __logf(l);
+        if (!DELTA && valid && a.lse) a.lse[bh * a.Nq + grow] = m * 0.69314718055994531f + __logf(l);
         tc_fence_before();
         mbar_arrive(&bars->ofree[rb]);
       }
@@ -332,6 +386,11 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ts_w(d_tmem, a_tmem + kk * 8, vs_lo + ((kk * 2048) >> 4), v_hi, kIdescPV,
                      (!first || kk > 0) ? 1u : 0u);
+          if (DELTA) {  // the remainder of P, from the second half of the S buffer
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts_w(d_tmem, a_tmem + BN / 2 + kk * 8, vs_lo + ((kk * 2048) >> 4), v_hi, kIdescPV, 1u);
+          }
           mma_commit(&bars->pvdone[b][rb]);
         }
         mma_commit(&bars->vempty[s]);
@@ -430,7 +489,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         for (int i = 0; i < C::kKVRowsPerThread; ++i) {
           const int r = row0 + i * C::kRowStep;
           const int64_t pos = int64_t(jj) * BN + r;
-          if (r < BN && pos < len) dst[i] = __ldg(a.col_idx + begin + pos);
+          if (r < BN && pos < len) dst[i] = a.dense ? static_cast<int>(pos) : __ldg(a.col_idx + begin + pos);
         }
       };
       // Issue one tile's copies: rows past the list, and flagged indices
@@ -508,11 +567,11 @@ done:
   }
 }
 
-template <int D, int RB, int BN, int STAGES>
+template <int D, int RB, int BN, int STAGES, bool DELTA>
 static cudaError_t launch(const FwdArgs& a, const CUtensorMap& tmq, int num_sms,
                           cudaStream_t stream) {
   using C = FwdCfg<D, RB, BN, STAGES>;
-  auto kern = sa_forward_kernel<D, RB, BN, STAGES>;
+  auto kern = sa_forward_kernel<D, RB, BN, STAGES, DELTA>;
   // At least half the SM's shared memory, so that one CTA owns each SM's TMEM.
   const int smem = C::kSmemBytes > 120 * 1024 ? C::kSmemBytes : 120 * 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -522,17 +581,26 @@ static cudaError_t launch(const FwdArgs& a, const CUtensorMap& tmq, int num_sms,
   return cudaGetLastError();
 }
 
-cudaError_t launch_forward(const FwdArgs& a, int d, int num_sms, cudaStream_t stream) {
+template <bool DELTA>
+static cudaError_t launch_any(const FwdArgs& a, int d, int num_sms, cudaStream_t stream) {
   if (a.units <= 0) return cudaSuccess;
   const int64_t bh = a.units / a.G;
   CUtensorMap tmq;
   if (!make_rows_map(&tmq, a.q, uint64_t(bh) * a.Nq, d, 128)) return cudaErrorInvalidValue;
   if (d == 128) {
-    return a.M <= 128 ? launch<128, 1, 128, 3>(a, tmq, num_sms, stream)
-                      : launch<128, 2, 64, 4>(a, tmq, num_sms, stream);
+    return a.M <= 128 ? launch<128, 1, 128, 3, DELTA>(a, tmq, num_sms, stream)
+                      : launch<128, 2, 64, 4, DELTA>(a, tmq, num_sms, stream);
   }
-  return a.M <= 128 ? launch<64, 1, 128, 4>(a, tmq, num_sms, stream)
-                    : launch<64, 2, 64, 4>(a, tmq, num_sms, stream);
+  return a.M <= 128 ? launch<64, 1, 128, 4, DELTA>(a, tmq, num_sms, stream)
+                    : launch<64, 2, 64, 4, DELTA>(a, tmq, num_sms, stream);
+}
+
+cudaError_t launch_forward(const FwdArgs& a, int d, int num_sms, cudaStream_t stream) {
+  return launch_any<false>(a, d, num_sms, stream);
+}
+
+cudaError_t launch_forward_delta(const FwdArgs& a, int d, int num_sms, cudaStream_t stream) {
+  return launch_any<true>(a, d, num_sms, stream);
 }
 
 }  // namespace sa

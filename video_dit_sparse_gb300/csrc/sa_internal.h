@@ -23,9 +23,15 @@ struct FwdArgs {
   int32_t out_fp32;
   int32_t neg_scale;  // scale < 0: scores are negated and scale_log2 = |scale| log2(e)
   float scale_log2;   // |scale| * log2(e)
+  int32_t dense = 0;  // no lists: every unit keeps keys 0 .. Nk-1
+  // sparse delta (launch_forward_delta): o = base + sign * sum_j exp(l_ij - lse_i) v_j
+  const float* lse_ref = nullptr;  // [B,H,Nq] natural-log normaliser per query row
+  const float* base = nullptr;     // [B,H,Nq,d] fp32 or null (zero)
+  float sign = 1.f;
 };
 
 cudaError_t launch_forward(const FwdArgs& a, int d, int num_sms, cudaStream_t stream);
+cudaError_t launch_forward_delta(const FwdArgs& a, int d, int num_sms, cudaStream_t stream);
 
 // Index builder.  The workspace holds, in order (each 256-byte aligned):
 //   qhi, qlo   bf16 [rows, d]   mean query split as hi + lo
@@ -43,6 +49,11 @@ BuildLayout build_layout(int64_t rows, int32_t Nk, int32_t d);
 struct BuildArgs {
   const uint16_t* q;
   const uint16_t* k;
+  // dense-step lists: stat >= 0 ranks keys by ln max_i / ln sum_i of
+  // exp(scale q_i.k_j - lse_i) over the group's rows instead of the mean-query
+  // score, and THRESHOLD compares that statistic itself with the threshold
+  const float* lse = nullptr;
+  int32_t stat = -1;  // -1 mean query, 0 column max, 1 column sum
   int64_t* row_ptr;
   int32_t* col_idx;
   int64_t col_capacity;
