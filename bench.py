@@ -40,7 +40,13 @@ L2_FLUSH_BYTES = 512 << 20
 def kernels_per_step(mode: str) -> int:
     """Our kernels per step: mean query, scores, select, scan, [emit,] forward.
     TOPK lists are written by the select kernel; the other modes add the
-    emit kernel once the row offsets are known."""
+    emit kernel once the row offsets are known.  Dense-step workloads: dense
+    forward, column statistics, select, scan, [emit,] and the sparse forward
+    (cached mask) or the two sparse deltas (column sums, TOPK)."""
+    if mode == "cached":
+        return 6
+    if mode == "colsum":
+        return 6
     return 5 if mode == "topk" else 6
 
 
@@ -231,7 +237,9 @@ def run_reference(args, w):
 def workload_config(w, pairs):
     c = {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
          "group": w.group, "selection": {"topk": f"k={w.topk}", "mass": f"rho={w.mass}",
-                                         "threshold": f"tau={w.threshold}"}[w.mode],
+                                         "threshold": f"tau={w.threshold}",
+                                         "cached": f"column max >= {w.threshold:.4g}",
+                                         "colsum": f"column sum top k={w.topk}"}[w.mode],
          "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)"}
     if pairs is not None:
         c["kept_pairs"] = pairs
@@ -371,6 +379,160 @@ def run_ours(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_ours_dense(args, w):
+    """Dense-step workloads.  One step = the refresh of a cached mask and the
+    sparse work that follows it:
+      cached:  dense forward (o, lse) -> column max of the dense probabilities
+               >= tau (FG-Attn cached mask) -> sparse forward on those lists;
+      colsum:  dense forward (fp32 o, lse) -> column-sum top-k (Chipmunk)
+               -> sparse delta writing the cache (o - kept terms) -> sparse
+               delta adding the kept terms back (the next step's update).
+    value = 4*d*(kept pairs of every attention call) / step time."""
+    import torch
+    world, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from video_dit_sparse_gb300 import binding as sa
+    from video_dit_sparse_gb300 import inputs as I
+
+    x = I.make_inputs(w, 0)
+    dev = torch.device("cuda", local)
+
+    def host(b):
+        return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    hq, hk, hv = host(x["q"]), host(x["k"]), host(x["v"])
+    q, k, v = hq.to(dev), hk.to(dev), hv.to(dev)
+    stream = torch.cuda.current_stream()
+    cached = w.mode == "cached"
+    p = sa.problem(q, k, w.group, w.scale, torch.bfloat16 if cached else torch.float32)
+    ws = torch.empty(sa.sparse_attn_build_index_workspace_size(p), dtype=torch.uint8, device=dev)
+    rows = w.B * w.H * w.G
+    cap = rows * (w.Nk if cached else w.topk)
+    col = torch.empty(cap, dtype=torch.int32, device=dev)
+    row_ptr = torch.empty(rows + 1, dtype=torch.int64, device=dev)
+    o = torch.empty(q.shape, dtype=torch.bfloat16 if cached else torch.float32, device=dev)
+    o2 = torch.empty_like(o)
+    cache = torch.empty(q.shape, dtype=torch.float32, device=dev) if not cached else None
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if cached:
+        sel = sa.sa_select(sa.SA_SELECT_THRESHOLD, 0, w.threshold, 0.99)
+        stat = sa.SA_COLSTAT_MAX
+    else:
+        sel = sa.sa_select(sa.SA_SELECT_TOPK, w.topk, 0.0, 0.99)
+        stat = sa.SA_COLSTAT_SUM
+    P, S = sa.ctypes.byref(p), sa._stream(stream)
+
+    def check(st, where):
+        if st:
+            raise sa.SparseAttnError(st, where)
+
+    def dense():
+        check(sa.lib.sparse_attn_forward(P, sa._ptr(q), sa._ptr(k), sa._ptr(v), None, None, 0,
+                                         sa._ptr(o), sa._ptr(lse), None, S), "dense forward")
+
+    def build():
+        # capacity covers every key, so no synchronisation is needed for nnz
+        check(sa.lib.sparse_attn_build_index_dense(P, sa.ctypes.byref(sel), stat, sa._ptr(q),
+                                                   sa._ptr(k), sa._ptr(lse), sa._ptr(row_ptr),
+                                                   sa._ptr(col), cap, None, sa._ptr(ws),
+                                                   ws.numel(), S), "build_index_dense")
+
+    def sparse():
+        if cached:
+            check(sa.lib.sparse_attn_forward(P, sa._ptr(q), sa._ptr(k), sa._ptr(v), sa._ptr(row_ptr),
+                                             sa._ptr(col), cap, sa._ptr(o2), None, None, S),
+                  "sparse forward")
+        else:
+            check(sa.lib.sparse_attn_forward_delta(P, sa._ptr(q), sa._ptr(k), sa._ptr(v),
+                                                   sa._ptr(row_ptr), sa._ptr(col), cap, sa._ptr(lse),
+                                                   sa._ptr(o), -1.0, sa._ptr(cache), None, S),
+                  "delta (cache)")
+            check(sa.lib.sparse_attn_forward_delta(P, sa._ptr(q), sa._ptr(k), sa._ptr(v),
+                                                   sa._ptr(row_ptr), sa._ptr(col), cap, sa._ptr(lse),
+                                                   sa._ptr(cache), 1.0, sa._ptr(o2), None, S),
+                  "delta (update)")
+
+    for _ in range(max(args.warmup, 1)):
+        dense()
+        build()
+        sparse()
+    torch.cuda.synchronize()
+    pairs = kept_pairs(row_ptr.cpu().numpy(), w.B, w.H, w.Nq, w.group)
+    dense_pairs = w.B * w.H * w.Nq * w.Nk
+    sparse_calls = 1 if cached else 2
+    flops = 4.0 * w.d * (dense_pairs + sparse_calls * pairs)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            dense()
+            ev[i][1].record(stream)
+            build()
+            ev[i][2].record(stream)
+            sparse()
+            ev[i][3].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in ev])
+    t_dense, t_build, t_sparse = (float(x) for x in t.mean(axis=0))
+    ms_step = t_dense + t_build + t_sparse
+    ms_max, units_total = aggregate(ms_step, flops, world)
+    value = units_total / (ms_max * 1e-3) / 1e12
+
+    e2e_steps = max(3, min(args.steps, 10))
+    h_o = torch.empty(o2.shape, dtype=o2.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(e2e_steps):
+        flush.zero_()
+        e0.record(stream)
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        dense()
+        build()
+        sparse()
+        h_o.copy_(o2, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_ms_max, _ = aggregate(float(np.mean(e2e_ms)), 0.0, world)
+    if rank != 0:
+        return
+    pk, pk_kind = peaks()
+    achieved = 4.0 * w.d * dense_pairs / (t_dense * 1e-3) / 1e12
+    cs_flops = 2.0 * w.d * dense_pairs  # the column statistics' QK^T
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(w, pairs),
+            "ms_dense_forward": t_dense, "ms_build_index_dense": t_build,
+            ("ms_sparse_forward" if cached else "ms_delta_pair"): t_sparse,
+            "density": pairs / dense_pairs,
+            "gpu_launches": kernels_per_step(w.mode) * args.steps,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                         "kernel": "sa_forward_kernel (dense mode)",
+                         "peak_source": f"{pk_kind} bf16_tflops (burst)"},
+            "build_index_dense_tflops": cs_flops / (t_build * 1e-3) / 1e12,
+            "e2e": {"value": units_total / (e2e_ms_max * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(3 * q.numel() * 2),
+                    "d2h_bytes_per_step": int(o2.numel() * o2.element_size()),
+                    "ms_per_step": e2e_ms_max},
+            "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -386,6 +548,8 @@ def main():
     w = I.preset(args.workload)
     if args.impl == "reference":
         run_reference(args, w)
+    elif w.mode in ("cached", "colsum"):
+        run_ours_dense(args, w)
     else:
         run_ours(args, w)
 

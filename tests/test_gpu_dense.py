@@ -245,3 +245,50 @@ def test_cached_mask_69k_sampled():
     density = nnz / (rows * Nk)
     assert 0.0 < density < 1.0
     P.compare_units(x["q"], x["k"], x["v"], 128, rp.cpu().numpy(), col.cpu().numpy(), units, o_s, lse_s)
+
+
+def test_colsum_delta_chunk192_sampled():
+    """Chipmunk's dense step on the C = 192 chunk workload (69K tokens):
+    dense forward, column-sum top 10 %, the cache (o minus the kept keys'
+    terms) and the update that adds them back; sampled chunks checked by the
+    oracle."""
+    from video_dit_sparse_gb300 import binding as sa
+    w = I.preset("colsum192_top10")
+    x = P.cached_inputs("colsum192_top10")
+    qd, kd, vd = P.to_dev(x["q"]), P.to_dev(x["k"]), P.to_dev(x["v"])
+    o, lse = sa.sparse_attn_forward(qd, kd, vd, None, None, group_size=192, out_dtype=torch.float32)
+    rp, col, nnz = sa.sparse_attn_build_index_dense(qd, kd, lse, "sum", "topk", topk=w.topk,
+                                                    group_size=192)
+    cache = sa.sparse_attn_forward_delta(qd, kd, vd, rp, col, lse, base=o, sign=-1.0, group_size=192)
+    back = sa.sparse_attn_forward_delta(qd, kd, vd, rp, col, lse, base=cache, sign=1.0, group_size=192)
+    torch.cuda.synchronize()
+    rows = w.B * w.H * w.G
+    assert nnz == rows * w.topk
+    assert (back - o).abs().max().item() < 1e-4
+    units = np.sort(np.random.default_rng(8).choice(rows, size=3, replace=False)).astype(np.int64)
+    # the dense step of the sampled chunks: o and lse over every key
+    uset = set(units.tolist())
+    o_ref, lse_ref = oracle.forward(x["q"], x["k"], x["v"], 192, w.scale, *oracle.to_csr(
+        [np.arange(w.Nk, dtype=np.int32) if u in uset else np.zeros(0, np.int32)
+         for u in range(rows)]), units)
+    lse_full = np.zeros((w.B, w.H, w.Nq))
+    lse_all = lse.view(-1).cpu().numpy()
+    for i, u in enumerate(units):
+        h, g = u // w.G, u % w.G
+        lse_full[0, h, g * 192:(g + 1) * 192] = lse_ref[i]
+        got = lse_all[h * w.Nq + g * 192: h * w.Nq + (g + 1) * 192]
+        assert np.all(np.abs(got - lse_ref[i]) <= 1e-3 * np.maximum(np.abs(lse_ref[i]), 1.0))
+    lists, cut, st = oracle.dense_index(x["q"], x["k"], lse_full, 192, w.scale, "sum", "topk",
+                                        topk=w.topk, units=units)
+    P.compare_lists(rp, col, units, lists, cut, st, w.Nk)
+    # the cache of the sampled chunks, on the GPU's lists and lse
+    rpn, coln = rp.cpu().numpy(), col.cpu().numpy()
+    lse_gpu = lse.double().cpu().numpy()
+    d_ref = oracle.forward_delta(x["q"], x["k"], x["v"], 192, w.scale, rpn, coln, lse_gpu,
+                                 None, -1.0, units)
+    c_all = cache.view(w.B * w.H, w.Nq, w.d)
+    for i, u in enumerate(units):
+        h, g = u // w.G, u % w.G
+        got = c_all[h, g * 192:(g + 1) * 192].double().cpu().numpy()
+        err = np.abs(got - (o_ref[i] + d_ref[i]))
+        assert err.max() <= P.O_MAX and err.mean() <= P.O_MEAN, (u, err.max(), err.mean())

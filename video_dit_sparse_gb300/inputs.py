@@ -55,7 +55,10 @@ class Workload:
     Nq/Nk; ``q_frame_offset`` places the query grid inside the key grid's
     time axis (rolling-window KV: queries are the newest chunk).
     ``voxel`` is None for raster order.  ``mode`` is "topk", "threshold",
-    "mass" or "given" (index lists supplied by :func:`uniform_lists`).
+    "mass" or "given" (index lists supplied by :func:`uniform_lists`), or a
+    dense-step rule: "cached" (column max of the dense probabilities against
+    ``threshold``, FG-Attn's cached mask) or "colsum" (top ``keep_pct`` % by
+    column sums, Chipmunk's selection, followed by the sparse delta).
     """
     name: str
     B: int
@@ -126,6 +129,17 @@ for _p in (5, 10, 20, 40, 100):
     PRESETS[f"sweep69k_top{_p}"] = Workload(
         f"sweep69k_top{_p}", 1, 24, 128, 128, (18, 48, 80), (18, 48, 80),
         voxel=(2, 8, 8), keep_pct=float(_p))
+
+
+# Dense-step workloads on the 18x48x80 grid: the cached mask of the FG-Attn
+# review (keep a slice when one of its dense probabilities reaches 0.5/N,
+# M = 128) and Chipmunk's column-sum top 10 % over C = 192 chunks with the
+# sparse delta.
+PRESETS["cached69k"] = Workload("cached69k", 1, 24, 128, 128, (18, 48, 80), (18, 48, 80),
+                                voxel=(2, 8, 8), mode="cached", threshold=0.5 / 69120)
+PRESETS["colsum192_top10"] = Workload("colsum192_top10", 1, 24, 128, 192, (18, 48, 80),
+                                      (18, 48, 80), voxel=(3, 8, 8), mode="colsum",
+                                      keep_pct=10.0)
 
 
 def preset(name: str) -> Workload:
