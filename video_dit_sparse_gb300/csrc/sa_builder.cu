@@ -455,7 +455,7 @@ __device__ __forceinline__ void for_each_key(const float* s, int Nk, F&& f) {
 // k-1 as the cut; MASS the first key at which the running fixed-point mass
 // reaches `target`.  Returns the cut as (order key, kept ties, row count).
 template <class Src>
-__device__ void exact_select(const Src& src, float lo0, float hi0, int64_t k, double target,
+__device__ void exact_select(const Src& src, float lo0, float hi0, int64_t k, int64_t target,
                              bool by_mass, float rmax, int64_t above_cnt, int64_t above_mass,
                              int64_t keep_all_count, SelSmem& sm, uint32_t* cut, int32_t* ties,
                              int64_t* count) {
@@ -510,8 +510,8 @@ __device__ void exact_select(const Src& src, float lo0, float hi0, int64_t k, do
     for (int e = 0; e < kBinsPerThread; ++e) {
       const int bin = top - e;
       const int64_t bc = sm.hist[bin], bm = by_mass ? int64_t(sm.hmass[bin]) : 0;
-      const bool cross = by_mass ? (bm > 0 && double(cum_m + bm) >= target && double(cum_m) < target)
-                                 : (bc > 0 && double(cum_c + bc) >= target && double(cum_c) < target);
+      const bool cross = by_mass ? (bm > 0 && cum_m + bm >= target && cum_m < target)
+                                 : (bc > 0 && cum_c + bc >= target && cum_c < target);
       if (cross && atomicCAS(&sm.claim, -1, bin) == -1) {
         sm.found_cnt = static_cast<int32_t>(bc);
         sm.found_above_cnt = cum_c - above_cnt;
@@ -578,9 +578,9 @@ __device__ void exact_select(const Src& src, float lo0, float hi0, int64_t k, do
     *cut = order_key(xv);
     int32_t t;
     if (by_mass) {
-      const double e = static_cast<double>(fixed_mass(xv, rmax));
-      const double need = e > 0.0 ? ceil((target - double(above_mass)) / e) : 1.0;
-      t = static_cast<int32_t>(need < 1.0 ? 1 : (need > double(n_und) ? n_und : need));
+      const int64_t e = static_cast<int64_t>(fixed_mass(xv, rmax));
+      const int64_t need = e > 0 ? (target - above_mass + e - 1) / e : 1;
+      t = static_cast<int32_t>(need < 1 ? 1 : (need > n_und ? n_und : need));
     } else {
       t = static_cast<int32_t>(min64(k - above_cnt, n_und));
     }
@@ -603,7 +603,7 @@ __device__ void exact_select(const Src& src, float lo0, float hi0, int64_t k, do
     bool is_cut;
     if (by_mass) {
       const int64_t incl = above_mass + before_m + int64_t(fixed_mass(xc, rmax));
-      is_cut = double(incl) >= target && double(above_mass + before_m) < target;
+      is_cut = incl >= target && above_mass + before_m < target;
     } else {
       is_cut = above_cnt + rank == k - 1;
     }
@@ -824,7 +824,10 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
   } else {
     const int64_t k = min64(max64(a.topk, 1), Nk);
     float rmax = 0.f;
-    double target = static_cast<double>(k);
+    // Rank or fixed-point mass the cut must reach.  Every comparison below is
+    // between integers (FP64 is slow on this part): for an integer sum x,
+    // x >= mass * total  <=>  x >= ceil(mass * total).
+    int64_t target = k;
     if (by_mass) {
       float mx = -INFINITY;
       for_each_key(s, Nk, [&](int, float x) { mx = fmaxf(mx, x); });
@@ -833,7 +836,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
       for_each_key(s, Nk, [&](int, float x) { zt += fixed_mass(x, rmax); });
       int64_t ztot;
       block_excl_scan<int64_t>(static_cast<int64_t>(zt), &ztot, sm.scan_m);
-      target = a.mass * static_cast<double>(ztot);
+      target = static_cast<int64_t>(ceil(a.mass * static_cast<double>(ztot)));
     }
     // ---- bracket the cut from an evenly strided sample of the row
     float lo = -INFINITY, hi = INFINITY;
@@ -875,26 +878,26 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
         const int64_t cex = block_excl_scan<int64_t>(c4, &ctot, sm.scan_c);
         const int64_t mex = by_mass ? block_excl_scan<int64_t>(m4, &mtot, sm.scan_m) : 0;
         // expected rank of the cut among the samples, counted from the top
-        double p;
+        float p;
         if (by_mass) {
           if (tid == 0) sm.found_above_cnt = S;  // no crossing: bracket everything below the top
           __syncthreads();
-          const double share = a.mass * double(mtot);
+          const int64_t share = static_cast<int64_t>(ceil(a.mass * static_cast<double>(mtot)));
           int64_t cm = mex, cc = cex;
           for (int e = 0; e < kBinsPerThread; ++e) {
             const int64_t bm = int64_t(sm.hmass[top - e]), bc = sm.hist[top - e];
-            if (bm > 0 && double(cm + bm) >= share && double(cm) < share) sm.found_above_cnt = cc + bc;
+            if (bm > 0 && cm + bm >= share && cm < share) sm.found_above_cnt = cc + bc;
             cm += bm;
             cc += bc;
           }
           __syncthreads();
-          p = double(sm.found_above_cnt);
+          p = float(sm.found_above_cnt);
         } else {
-          p = double(k) * S / double(Nk);
+          p = float(k) * float(S) / float(Nk);
         }
-        const double q = fmin(fmax(p / S, 0.0), 1.0);
-        const double delta = 5.0 * sqrt(double(S) * q * (1.0 - q)) + 16.0;
-        const double r_hi = p - delta, r_lo = p + delta;  // sample ranks bounding the cut
+        const float q = fminf(fmaxf(p / float(S), 0.f), 1.f);
+        const float delta = 5.f * sqrtf(float(S) * q * (1.f - q)) + 16.f;
+        const float r_hi = p - delta, r_lo = p + delta;  // sample ranks bounding the cut
         if (tid == 0) {
           sm.fred[2][0] = INFINITY;
           sm.fred[2][1] = -INFINITY;
@@ -905,13 +908,13 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
           const int bn = top - e;
           const int64_t bc = sm.hist[bn];
           // this bin covers sample ranks [cc, cc + bc)
-          if (bc > 0 && r_hi >= double(cc) && r_hi < double(cc + bc)) sm.fred[2][0] = smn + float(bn + 1) / inv;
-          if (bc > 0 && r_lo >= double(cc) && r_lo < double(cc + bc)) sm.fred[2][1] = smn + float(bn) / inv;
+          if (bc > 0 && r_hi >= float(cc) && r_hi < float(cc + bc)) sm.fred[2][0] = smn + float(bn + 1) / inv;
+          if (bc > 0 && r_lo >= float(cc) && r_lo < float(cc + bc)) sm.fred[2][1] = smn + float(bn) / inv;
           cc += bc;
         }
         __syncthreads();
-        hi = r_hi >= 0.0 ? sm.fred[2][0] : INFINITY;
-        lo = r_lo < double(S) ? sm.fred[2][1] : -INFINITY;
+        hi = r_hi >= 0.f ? sm.fred[2][0] : INFINITY;
+        lo = r_lo < float(S) ? sm.fred[2][1] : -INFINITY;
       } else {
         lo = hi = smn;  // flat sample: try its single value, fall back if wrong
       }
@@ -1002,7 +1005,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
     }
     const int n_win = sm.n_win;
     const bool bracketed =
-        n_win <= kWindow && (by_mass ? (double(above_mass) < target && target <= double(above_mass + win_mass))
+        n_win <= kWindow && (by_mass ? (above_mass < target && target <= above_mass + win_mass)
                                      : (above_cnt < k && k <= above_cnt + n_win));
     // A window of at most kWindow/2 keys gets its scores copied next to the
     // indices (one gather from L2), so the selection passes read shared memory.

@@ -93,9 +93,10 @@ struct FwdBars {
 };
 
 // Unit u's list bounds.  A malformed row_ptr pair makes the unit empty.
+template <bool DENSE>
 __device__ __forceinline__ int64_t unit_list(const FwdArgs& a, int64_t u, int64_t* begin,
                                              bool* bad) {
-  if (a.dense) {
+  if (DENSE) {
     *bad = false;
     *begin = 0;
     return a.Nk;
@@ -145,7 +146,9 @@ __device__ __forceinline__ void store_row32(const FwdArgs& a, int64_t orow_off, 
   }
 }
 
-template <int D, int RB, int BN, int STAGES, bool DELTA>
+// DENSE (no lists) is a template parameter: a run-time choice inside the
+// gather warps' index loads costs a fifth of the sparse kernel's speed.
+template <int D, int RB, int BN, int STAGES, bool DELTA, bool DENSE>
 __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     sa_forward_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq) {
   using C = FwdCfg<D, RB, BN, STAGES>;
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
       int64_t begin;
       bool bad;
-      const int64_t len = unit_list(a, u, &begin, &bad);
+      const int64_t len = unit_list<DENSE>(a, u, &begin, &bad);
       if (bad && threadIdx.x == 0) report(a.status, SA_DEVERR_ROW_PTR);
       const int64_t bh = u / G, g = u % G;
       const int64_t grow = g * a.M + row_in_unit;
@@ -399,7 +402,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
       for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
         int64_t begin;
         bool bad;
-        const int64_t len = unit_list(a, u, &begin, &bad);
+        const int64_t len = unit_list<DENSE>(a, u, &begin, &bad);
         const uint32_t n = static_cast<uint32_t>((len + BN - 1) / BN);
         if (n == 0) continue;
         if (!mbar_wait(&bars->qfull, un & 1, abort)) break;
@@ -478,7 +481,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
       int64_t begin;
       bool bad;
-      const int64_t len = unit_list(a, u, &begin, &bad);
+      const int64_t len = unit_list<DENSE>(a, u, &begin, &bad);
       const uint32_t n = static_cast<uint32_t>((len + BN - 1) / BN);
       if (n == 0) continue;
       const int64_t bh = u / G, g = u % G;
@@ -489,7 +492,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         for (int i = 0; i < C::kKVRowsPerThread; ++i) {
           const int r = row0 + i * C::kRowStep;
           const int64_t pos = int64_t(jj) * BN + r;
-          if (r < BN && pos < len) dst[i] = a.dense ? static_cast<int>(pos) : __ldg(a.col_idx + begin + pos);
+          if (r < BN && pos < len) dst[i] = DENSE ? static_cast<int>(pos) : __ldg(a.col_idx + begin + pos);
         }
       };
       // Issue one tile's copies: rows past the list, and flagged indices
@@ -571,7 +574,8 @@ template <int D, int RB, int BN, int STAGES, bool DELTA>
 static cudaError_t launch(const FwdArgs& a, const CUtensorMap& tmq, int num_sms,
                           cudaStream_t stream) {
   using C = FwdCfg<D, RB, BN, STAGES>;
-  auto kern = sa_forward_kernel<D, RB, BN, STAGES, DELTA>;
+  auto kern = a.dense ? sa_forward_kernel<D, RB, BN, STAGES, DELTA, true>
+                      : sa_forward_kernel<D, RB, BN, STAGES, DELTA, false>;
   // At least half the SM's shared memory, so that one CTA owns each SM's TMEM.
   const int smem = C::kSmemBytes > 120 * 1024 ? C::kSmemBytes : 120 * 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
