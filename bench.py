@@ -543,9 +543,14 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="run the workload with this many heads (smaller ncu captures)")
     args = ap.parse_args()
     from video_dit_sparse_gb300 import inputs as I
     w = I.preset(args.workload)
+    if args.heads > 0:
+        import dataclasses
+        w = dataclasses.replace(w, H=args.heads, name=f"{w.name}_h{args.heads}")
     if args.impl == "reference":
         run_reference(args, w)
     elif w.mode in ("cached", "colsum"):
