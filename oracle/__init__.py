@@ -265,3 +265,58 @@ def forward_delta(q, k, v, M: int, scale: float, row_ptr, col_idx, lse, base=Non
     if rc:
         raise ValueError("oracle_forward_delta rejected its arguments")
     return o
+
+
+# ------------------------------------------------------------ token layout
+# Chipmunk review, "What carries the argument" / Alg. 1 (voxel reordering):
+# tokens of a (T, Hh, W) latent grid are reordered so that contiguous chunks
+# are spatio-temporal voxels.  Reading: voxels of (vt, vh, vw) tokens in
+# raster order over the voxel grid, tokens raster-ordered inside each voxel;
+# at the grid's far edges voxels are clipped to what remains.
+
+def voxel_order(grid, voxel):
+    """order[n] = raster index (t*Hh*W + h*W + w) of the token at position n
+    of the voxel-ordered sequence; built by enumerating voxels one by one."""
+    T, Hh, W = grid
+    vt, vh, vw = voxel
+    order = []
+    for t0 in range(0, T, vt):
+        for h0 in range(0, Hh, vh):
+            for w0 in range(0, W, vw):
+                for t in range(t0, min(t0 + vt, T)):
+                    for h in range(h0, min(h0 + vh, Hh)):
+                        for w in range(w0, min(w0 + vw, W)):
+                            order.append((t * Hh + h) * W + w)
+    return np.asarray(order, dtype=np.int64)
+
+
+def voxel_permute(x, grid, voxel, inverse: bool = False):
+    """x [..., N, d] (any dtype): raster -> voxel order (y[n] = x[order[n]]),
+    or back (y[order[n]] = x[n]) when inverse."""
+    order = voxel_order(grid, voxel)
+    if inverse:
+        y = np.empty_like(x)
+        y[..., order, :] = x
+        return y
+    return x[..., order, :]
+
+
+# DiT page, "The Architecture" (KV window of 4 chunks: the first chunk is a
+# permanent attention sink, then the 2 most recent chunks and the current one)
+# and its per-chunk loop ("roll the cache if the 4-chunk window is full (sink
+# stays)").  Reading: the cache holds S chunk slots in chronological order.
+
+def kv_window_append(cache, new, chunks_before: int):
+    """cache [..., S*L, d], new [..., L, d]; returns (cache after appending the
+    chunk, number of valid key tokens).  While slots are free the chunk fills
+    the next one; once full, slot 0 (the sink) stays, every other chunk moves
+    one slot towards the sink (the oldest non-sink chunk leaves) and the new
+    chunk takes the last slot."""
+    L = new.shape[-2]
+    S = cache.shape[-2] // L
+    chunks = [cache[..., s * L:(s + 1) * L, :].copy() for s in range(S)]
+    if chunks_before < S:
+        chunks[chunks_before] = new.copy()
+    else:
+        chunks = [chunks[0]] + chunks[2:] + [new.copy()]
+    return np.concatenate(chunks, axis=-2), min(chunks_before + 1, S) * L

@@ -102,3 +102,45 @@ def test_pins_catch_mutation(name, tmp_path, monkeypatch):
         except AssertionError:
             caught += 1
     assert caught > 0, f"no pin detects: {name}"
+
+
+# Planted mistakes in the oracle's Python layout functions: each is applied to
+# the function's source, the mutant replaces the real one, and a pin of
+# test_oracle_layout.py must fail.
+from tests import test_oracle_layout as lpins  # noqa: E402
+
+PY_MUTATIONS = {
+    "voxel loops h and w swapped": ("voxel_order", "for h in range(h0, min(h0 + vh, Hh)):\n                        for w in range(w0, min(w0 + vw, W)):",
+                                    "for w in range(w0, min(w0 + vw, W)):\n                        for h in range(h0, min(h0 + vh, Hh)):"),
+    "voxel edge not clipped": ("voxel_order", "min(t0 + vt, T)", "t0 + vt"),
+    "voxel raster index wrong": ("voxel_order", "(t * Hh + h) * W + w", "(t * W + h) * Hh + w"),
+    "inverse applies forward": ("voxel_permute", "y[..., order, :] = x", "y = x[..., order, :]"),
+    "window drops the sink": ("kv_window_append", "chunks = [chunks[0]] + chunks[2:] + [new.copy()]",
+                              "chunks = chunks[1:] + [new.copy()]"),
+    "window fills one slot late": ("kv_window_append", "if chunks_before < S:", "if chunks_before < S - 1:"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTATIONS))
+def test_layout_pins_catch_mutation(name, monkeypatch):
+    import inspect
+    import textwrap
+    fn, old, new = PY_MUTATIONS[name]
+    src = textwrap.dedent(inspect.getsource(getattr(oracle, fn)))
+    assert src.count(old) == 1, f"mutation anchor for {name!r} not unique"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), ns)
+    monkeypatch.setattr(oracle, fn, ns[fn])
+    if fn == "voxel_order":
+        monkeypatch.setattr(oracle, "voxel_permute", ns["voxel_permute"])
+    pins_ = [lambda: lpins.test_voxel_order_closed_form((4, 8, 8), (2, 4, 4)),
+             lambda: lpins.test_voxel_order_clipped_edges((5, 7, 9), (2, 3, 4)),
+             lambda: lpins.test_voxel_permute_inverse_and_generator_agree(),
+             lambda: lpins.test_kv_window_append_bruteforce(4)]
+    caught = 0
+    for pin in pins_:
+        try:
+            pin()
+        except (AssertionError, IndexError, ValueError):
+            caught += 1
+    assert caught > 0, f"no pin detects: {name}"
