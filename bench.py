@@ -533,6 +533,82 @@ def run_ours_dense(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_layout(args, w):
+    """Token-layout workloads, bound by HBM bandwidth.  voxel69k: one step
+    reorders Q, K and V into voxel order and O back to raster order (4 calls);
+    kvwindow_rollingkv: one step appends a chunk to the full 4-slot K/V
+    window (the sink stays, the other chunks roll).  value = bytes read +
+    written per step / step time."""
+    import torch
+    world, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from video_dit_sparse_gb300 import binding as sa
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+
+    def rnd(*shape):
+        return torch.randn(*shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if w.mode == "layout":
+        grid, voxel = w.grid_q, w.voxel
+        xs = [rnd(w.B, w.H, w.Nq, w.d) for _ in range(4)]
+        ys = [torch.empty_like(x) for x in xs]
+
+        def step():
+            for i, (x, y) in enumerate(zip(xs, ys)):
+                sa.sparse_attn_voxel_permute(x, grid, voxel, inverse=(i == 3), out=y, stream=stream)
+
+        step_bytes = sum(2 * x.numel() * 2 for x in xs)
+        calls, kernel = 4, "sa_voxel_permute_kernel"
+    else:
+        L = w.Nq  # one chunk: the newest 8 frames
+        S = w.Nk // L
+        ck, cv = rnd(w.B, w.H, S * L, w.d), rnd(w.B, w.H, S * L, w.d)
+        nk, nv = rnd(w.B, w.H, L, w.d), rnd(w.B, w.H, L, w.d)
+
+        def step():
+            sa.sparse_attn_kv_window_append(ck, cv, nk, nv, S + 3, stream=stream)
+
+        chunk = nk.numel() * 2
+        step_bytes = 2 * (chunk + 2 * (S - 2) * chunk + chunk)  # K and V: new read, rolls read+write, last slot write
+        calls, kernel = 1, "sa_kv_window_kernel"
+    for _ in range(max(args.warmup, 1)):
+        step()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    ms_max, bytes_total = aggregate(ms, float(step_bytes), world)
+    if rank != 0:
+        return
+    pk, pk_kind = peaks()
+    gbs = bytes_total / (ms_max * 1e-3) / 1e9
+    line = {"metric": "GB/s moved by the token-layout kernels (bytes read + written)", "value": gbs,
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)"},
+            "gpu_launches": calls * args.steps,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": kernel,
+                         "peak_source": f"{pk_kind} hbm_gbs"},
+            "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -555,6 +631,8 @@ def main():
         run_reference(args, w)
     elif w.mode in ("cached", "colsum"):
         run_ours_dense(args, w)
+    elif w.mode in ("layout", "kvwindow"):
+        run_layout(args, w)
     else:
         run_ours(args, w)
 

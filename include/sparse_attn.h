@@ -267,6 +267,50 @@ sa_status sparse_attn_forward_delta(const sa_problem* problem, const void* q, co
                                     sa_stream_t stream);
 
 /*
+ * Token layout on either side of the attention path.
+ *
+ * Voxel reordering (Chipmunk review, "What carries the argument" / Alg. 1):
+ * tokens of a (T, Hh, W) latent grid, raster order t*Hh*W + h*W + w, are
+ * reordered so that each contiguous run of vt*vh*vw tokens is one voxel:
+ * voxels in raster order over the voxel grid, tokens in raster order inside
+ * a voxel; voxels at the far edges of a grid they do not tile are clipped.
+ * With voxels of M (or C) tokens, query group g of the reordered sequence is
+ * voxel g.
+ *   grid      T, Hh, W >= 1 and the voxel vt, vh, vw >= 1; N = T*Hh*W < 2^31
+ *   x, y      device bf16 [BH, N, d], 16-byte aligned, not overlapping
+ *   inverse   0: y[n] = x[order[n]] (raster -> voxel), 1: y[order[n]] = x[n]
+ * d in {64, 128}.  Asynchronous; errors as for the other entry points.
+ */
+typedef struct {
+  int32_t T, Hh, W;    /* latent grid (frames, height, width in tokens) */
+  int32_t vt, vh, vw;  /* voxel shape */
+} sa_voxel_grid;
+
+sa_status sparse_attn_voxel_permute(const sa_voxel_grid* grid, int32_t BH, int32_t d, const void* x,
+                                    void* y, int32_t inverse, sa_stream_t stream);
+
+/*
+ * Rolling KV window (DiT page, "The Architecture": a window of 4 chunks,
+ * the first chunk a permanent attention sink, then the 2 most recent chunks
+ * and the current one; "roll the cache if the 4-chunk window is full (sink
+ * stays)").  The caches hold `slots` chunks of chunk_tokens rows in
+ * chronological order.  Appending the chunk numbered chunks_before (0 for
+ * the first): while chunks_before < slots it fills slot chunks_before;
+ * otherwise slots 1 .. slots-2 take the contents of slots 2 .. slots-1 (the
+ * oldest non-sink chunk leaves), the new chunk fills the last slot and slot
+ * 0 never changes.  K and V move alike, in place.
+ *   cache_k, cache_v  device bf16 [BH, slots * chunk_tokens, d], 16-byte aligned
+ *   new_k, new_v      device bf16 [BH, chunk_tokens, d], 16-byte aligned
+ *   valid_tokens      host, nullable: keys valid after the append,
+ *                     min(chunks_before + 1, slots) * chunk_tokens
+ * 2 <= slots <= 64; d in {64, 128}.  Asynchronous.
+ */
+sa_status sparse_attn_kv_window_append(int32_t BH, int32_t d, int32_t chunk_tokens, int32_t slots,
+                                       int64_t chunks_before, void* cache_k, void* cache_v,
+                                       const void* new_k, const void* new_v,
+                                       int64_t* valid_tokens, sa_stream_t stream);
+
+/*
  * Checks index lists without trapping: row_ptr[0] == 0, row_ptr[rows] == nnz,
  * row_ptr non-decreasing, every index in [0, Nk) and strictly ascending
  * within its row.  dev_status is a caller-provided device int32 used as the

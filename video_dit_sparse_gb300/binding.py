@@ -46,6 +46,11 @@ class sa_select(ctypes.Structure):
                 ("threshold", ctypes.c_double), ("mass", ctypes.c_double)]
 
 
+class sa_voxel_grid(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("Hh", ctypes.c_int32), ("W", ctypes.c_int32),
+                ("vt", ctypes.c_int32), ("vh", ctypes.c_int32), ("vw", ctypes.c_int32)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -67,6 +72,13 @@ def _load():
     lib.sparse_attn_forward_delta.argtypes = [P(sa_problem), vp, vp, vp, vp, vp, i64, vp, vp,
                                               ctypes.c_float, vp, vp, vp]
     lib.sparse_attn_forward_delta.restype = ctypes.c_int
+    lib.sparse_attn_voxel_permute.argtypes = [P(sa_voxel_grid), ctypes.c_int32, ctypes.c_int32, vp,
+                                              vp, ctypes.c_int32, vp]
+    lib.sparse_attn_voxel_permute.restype = ctypes.c_int
+    lib.sparse_attn_kv_window_append.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.c_int32, i64, vp, vp, vp, vp,
+                                                 P(ctypes.c_int64), vp]
+    lib.sparse_attn_kv_window_append.restype = ctypes.c_int
     lib.sparse_attn_validate_index.argtypes = [P(sa_problem), vp, vp, i64, vp, vp]
     lib.sparse_attn_validate_index.restype = ctypes.c_int
     lib.sparse_attn_status_string.argtypes = [ctypes.c_int]
@@ -280,9 +292,50 @@ def sparse_attn_validate_index(row_ptr: torch.Tensor, col_idx: torch.Tensor, *, 
     return st
 
 
+def sparse_attn_voxel_permute(x: torch.Tensor, grid, voxel, *, inverse: bool = False,
+                              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """x bf16 [B, H, N, d] (N = T*Hh*W) -> the same tokens in voxel order
+    (or back to raster order when inverse)."""
+    _check(x, torch.bfloat16, "x")
+    if x.dim() != 4:
+        raise ValueError("x must be [B, H, N, d]")
+    B, H, N, d = x.shape
+    g = sa_voxel_grid(*grid, *voxel)
+    if out is None:
+        out = torch.empty_like(x)
+    _check(out, torch.bfloat16, "out")
+    st = lib.sparse_attn_voxel_permute(ctypes.byref(g), B * H, d, _ptr(x), _ptr(out),
+                                       1 if inverse else 0, _stream(stream))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_voxel_permute")
+    return out
+
+
+def sparse_attn_kv_window_append(cache_k: torch.Tensor, cache_v: torch.Tensor,
+                                 new_k: torch.Tensor, new_v: torch.Tensor, chunks_before: int, *,
+                                 stream=None) -> int:
+    """Appends one chunk ([B, H, L, d]) to the rolling caches ([B, H, S*L, d],
+    slot 0 = sink) in place; returns the number of valid key tokens."""
+    for t, n in ((cache_k, "cache_k"), (cache_v, "cache_v"), (new_k, "new_k"), (new_v, "new_v")):
+        _check(t, torch.bfloat16, n)
+    B, H, SL, d = cache_k.shape
+    L = new_k.shape[2]
+    if cache_v.shape != cache_k.shape or new_v.shape != new_k.shape or SL % L:
+        raise ValueError("caches must be [B, H, S*L, d] and chunks [B, H, L, d]")
+    valid = ctypes.c_int64(0)
+    st = lib.sparse_attn_kv_window_append(B * H, d, L, SL // L, int(chunks_before), _ptr(cache_k),
+                                          _ptr(cache_v), _ptr(new_k), _ptr(new_v),
+                                          ctypes.byref(valid), _stream(stream))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_kv_window_append")
+    return int(valid.value)
+
+
 # Short aliases for Python callers.
 build_index = sparse_attn_build_index
 build_index_dense = sparse_attn_build_index_dense
 forward = sparse_attn_forward
 forward_delta = sparse_attn_forward_delta
 validate_index = sparse_attn_validate_index
+voxel_permute = sparse_attn_voxel_permute
+kv_window_append = sparse_attn_kv_window_append

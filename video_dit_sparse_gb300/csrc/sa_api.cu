@@ -311,6 +311,69 @@ sa_status sparse_attn_forward_delta(const sa_problem* p, const void* q, const vo
   return map_cuda(sa::launch_forward_delta(a, p->d, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+sa_status sparse_attn_voxel_permute(const sa_voxel_grid* g, int32_t BH, int32_t d, const void* x,
+                                    void* y, int32_t inverse, sa_stream_t stream) {
+  if (!g || BH < 1 || !x || !y || (inverse != 0 && inverse != 1)) return SA_ERR_INVALID_ARG;
+  if (g->T < 1 || g->Hh < 1 || g->W < 1 || g->vt < 1 || g->vh < 1 || g->vw < 1) return SA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return SA_ERR_UNSUPPORTED;
+  const int64_t N = int64_t(g->T) * g->Hh * g->W;
+  if (N >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(y, 16)) return SA_ERR_INVALID_ARG;
+  int sms = 0;
+  sa_status st = device_info(&sms);
+  if (st != SA_OK) return st;
+  const uint64_t bytes = uint64_t(BH) * uint64_t(N) * uint64_t(d) * 2;
+  if (!in_device_allocation(x, bytes) || !in_device_allocation(y, bytes)) return SA_ERR_INVALID_ARG;
+  const uintptr_t x0 = reinterpret_cast<uintptr_t>(x), y0 = reinterpret_cast<uintptr_t>(y);
+  if (x0 < y0 + bytes && y0 < x0 + bytes) return SA_ERR_INVALID_ARG;  // out of place only
+  sa::VoxArgs a;
+  a.x = static_cast<const uint4*>(x);
+  a.y = static_cast<uint4*>(y);
+  a.BH = BH;
+  a.N = static_cast<uint32_t>(N);
+  a.T = g->T;
+  a.Hh = g->Hh;
+  a.W = g->W;
+  a.vt = g->vt;
+  a.vh = g->vh;
+  a.vw = g->vw;
+  a.pieces = d / 8;
+  a.inverse = inverse;
+  return map_cuda(sa::launch_voxel_permute(a, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sa_status sparse_attn_kv_window_append(int32_t BH, int32_t d, int32_t chunk_tokens, int32_t slots,
+                                       int64_t chunks_before, void* cache_k, void* cache_v,
+                                       const void* new_k, const void* new_v,
+                                       int64_t* valid_tokens, sa_stream_t stream) {
+  if (BH < 1 || chunk_tokens < 1 || slots < 2 || slots > 64 || chunks_before < 0) return SA_ERR_INVALID_ARG;
+  if (!cache_k || !cache_v || !new_k || !new_v) return SA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return SA_ERR_UNSUPPORTED;
+  if (!aligned(cache_k, 16) || !aligned(cache_v, 16) || !aligned(new_k, 16) || !aligned(new_v, 16))
+    return SA_ERR_INVALID_ARG;
+  int sms = 0;
+  sa_status st = device_info(&sms);
+  if (st != SA_OK) return st;
+  const uint64_t chunk = uint64_t(BH) * uint64_t(chunk_tokens) * uint64_t(d) * 2;
+  const uint64_t cache = chunk * uint64_t(slots);
+  if (!in_device_allocation(cache_k, cache) || !in_device_allocation(cache_v, cache) ||
+      !in_device_allocation(new_k, chunk) || !in_device_allocation(new_v, chunk))
+    return SA_ERR_INVALID_ARG;
+  sa::KvArgs a;
+  a.ck = static_cast<uint4*>(cache_k);
+  a.cv = static_cast<uint4*>(cache_v);
+  a.nk = static_cast<const uint4*>(new_k);
+  a.nv = static_cast<const uint4*>(new_v);
+  a.BH = BH;
+  a.L16 = int64_t(chunk_tokens) * d / 8;
+  a.S = slots;
+  a.slot = chunks_before < slots ? static_cast<int32_t>(chunks_before) : -1;
+  if ((st = map_cuda(sa::launch_kv_window(a, sms, reinterpret_cast<cudaStream_t>(stream)))) != SA_OK)
+    return st;
+  if (valid_tokens) *valid_tokens = int64_t(chunks_before + 1 < slots ? chunks_before + 1 : slots) * chunk_tokens;
+  return SA_OK;
+}
+
 sa_status sparse_attn_validate_index(const sa_problem* p, const int64_t* row_ptr,
                                      const int32_t* col_idx, int64_t nnz, int32_t* dev_status,
                                      sa_stream_t stream) {

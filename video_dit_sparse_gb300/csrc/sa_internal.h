@@ -69,6 +69,29 @@ struct BuildArgs {
 
 cudaError_t launch_build_index(const BuildArgs& a, int num_sms, cudaStream_t stream);
 
+// Voxel reordering of [BH, N, d] bf16 rows (N = T*Hh*W < 2^31).
+struct VoxArgs {
+  const uint4* x;
+  uint4* y;
+  int64_t BH;
+  uint32_t N, T, Hh, W, vt, vh, vw;
+  int32_t pieces;   // 16-byte pieces per row: d / 8 (a divisor of 32)
+  int32_t inverse;  // 0: raster -> voxel order, 1: back
+};
+cudaError_t launch_voxel_permute(const VoxArgs& a, int num_sms, cudaStream_t stream);
+
+// Rolling KV window append of one chunk to caches of S slots.
+struct KvArgs {
+  uint4* ck;
+  uint4* cv;
+  const uint4* nk;
+  const uint4* nv;
+  int64_t BH, L16;  // heads; 16-byte pieces per chunk per head
+  int32_t S;        // slots (>= 2)
+  int32_t slot;     // slot to fill, or -1: roll (sink stays) and fill the last
+};
+cudaError_t launch_kv_window(const KvArgs& a, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_validate(const int64_t* row_ptr, const int32_t* col_idx, int64_t rows,
                             int64_t nnz, int32_t Nk, int32_t* status, cudaStream_t stream);
 

@@ -142,6 +142,15 @@ PRESETS["colsum192_top10"] = Workload("colsum192_top10", 1, 24, 128, 192, (18, 4
                                       keep_pct=10.0)
 
 
+# Token-layout workloads: voxel reordering of Q, K, V and back of O on the
+# 69K grid ((3,8,8) voxels, C = 192), and rolling-window appends of one
+# LongLive chunk (8 frames x 22x40 = 7040 tokens) to 4-slot K/V caches.
+PRESETS["voxel69k"] = Workload("voxel69k", 1, 24, 128, 192, (18, 48, 80), (18, 48, 80),
+                               voxel=(3, 8, 8), mode="layout")
+PRESETS["kvwindow_rollingkv"] = Workload("kvwindow_rollingkv", 1, 12, 128, 128, (8, 22, 40),
+                                         (32, 22, 40), mode="kvwindow")
+
+
 def preset(name: str) -> Workload:
     return PRESETS[name]
 
