@@ -320,3 +320,37 @@ def kv_window_append(cache, new, chunks_before: int):
     else:
         chunks = [chunks[0]] + chunks[2:] + [new.copy()]
     return np.concatenate(chunks, axis=-2), min(chunks_before + 1, S) * L
+
+
+# ------------------------------------------------------------ index formats
+# Chipmunk review, "Bitpacked Sparsity Masks": a boolean keep-mask stored one
+# bit per entry (8x smaller than one byte per entry).  Reading: per index row
+# (query group), ceil(Nk/32) little-endian uint32 words, key j is bit j % 32 of
+# word j // 32; bits past Nk are ignored.
+# FG-Attn review, "The pith" and Fig. 6: block-sparse masks (M x M tiles) can
+# be fed to the slice kernel.  Reading: a byte per (query group, key block of
+# block_k keys); a kept block keeps all of its keys (the last block ragged).
+
+def lists_from_bitmask(words, Nk: int):
+    """words uint32 [rows, ceil(Nk/32)] -> ascending key lists per row."""
+    words = np.ascontiguousarray(words, dtype=np.uint32)
+    out = []
+    for r in range(words.shape[0]):
+        keep = []
+        for j in range(Nk):
+            if (int(words[r, j // 32]) >> (j % 32)) & 1:
+                keep.append(j)
+        out.append(np.asarray(keep, dtype=np.int32))
+    return out
+
+
+def lists_from_block_mask(blocks, Nk: int, block_k: int):
+    """blocks uint8 [rows, ceil(Nk/block_k)] (non-zero = kept) -> key lists."""
+    out = []
+    for r in range(blocks.shape[0]):
+        keep = []
+        for b in range(blocks.shape[1]):
+            if blocks[r, b]:
+                keep.extend(range(b * block_k, min((b + 1) * block_k, Nk)))
+        out.append(np.asarray(keep, dtype=np.int32))
+    return out

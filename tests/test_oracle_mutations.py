@@ -107,6 +107,7 @@ def test_pins_catch_mutation(name, tmp_path, monkeypatch):
 # Planted mistakes in the oracle's Python layout functions: each is applied to
 # the function's source, the mutant replaces the real one, and a pin of
 # test_oracle_layout.py must fail.
+from tests import test_oracle_formats as fpins  # noqa: E402
 from tests import test_oracle_layout as lpins  # noqa: E402
 
 PY_MUTATIONS = {
@@ -118,6 +119,10 @@ PY_MUTATIONS = {
     "window drops the sink": ("kv_window_append", "chunks = [chunks[0]] + chunks[2:] + [new.copy()]",
                               "chunks = chunks[1:] + [new.copy()]"),
     "window fills one slot late": ("kv_window_append", "if chunks_before < S:", "if chunks_before < S - 1:"),
+    "bitmask bit order reversed": ("lists_from_bitmask", ">> (j % 32)", ">> (31 - j % 32)"),
+    "bitmask word index wrong": ("lists_from_bitmask", "words[r, j // 32]", "words[r, min(j // 8, words.shape[1] - 1)]"),
+    "block range not clipped": ("lists_from_block_mask", "min((b + 1) * block_k, Nk)", "(b + 1) * block_k"),
+    "block keeps from the wrong start": ("lists_from_block_mask", "range(b * block_k,", "range(b * block_k + 1,"),
 }
 
 
@@ -136,7 +141,10 @@ def test_layout_pins_catch_mutation(name, monkeypatch):
     pins_ = [lambda: lpins.test_voxel_order_closed_form((4, 8, 8), (2, 4, 4)),
              lambda: lpins.test_voxel_order_clipped_edges((5, 7, 9), (2, 3, 4)),
              lambda: lpins.test_voxel_permute_inverse_and_generator_agree(),
-             lambda: lpins.test_kv_window_append_bruteforce(4)]
+             lambda: lpins.test_kv_window_append_bruteforce(4),
+             lambda: fpins.test_bitmask_matches_numpy_packbits(7, 100, 0.3),
+             lambda: fpins.test_block_mask_matches_numpy_repeat(4, 100, 16),
+             lambda: fpins.test_block_sparse_attention_is_sdpa_with_block_mask()]
     caught = 0
     for pin in pins_:
         try:
