@@ -534,11 +534,12 @@ def run_ours_dense(args, w):
 
 
 def run_layout(args, w):
-    """Token-layout workloads, bound by HBM bandwidth.  voxel69k: one step
-    reorders Q, K and V into voxel order and O back to raster order (4 calls);
-    kvwindow_rollingkv: one step appends a chunk to the full 4-slot K/V
-    window (the sink stays, the other chunks roll).  value = bytes read +
-    written per step / step time."""
+    """Layout and index-format workloads, bound by HBM bandwidth.  voxel69k:
+    one step reorders Q, K and V into voxel order and O back to raster order
+    (4 calls); kvwindow_rollingkv: one step appends a chunk to the full 4-slot
+    K/V window (the sink stays, the other chunks roll); bitmask69k_top20 /
+    blockmask69k_top20: one step converts a keep-mask into CSR lists.
+    value = algorithmic bytes read + written per step / step time."""
     import torch
     world, rank, local = dist_info()
     torch.cuda.set_device(local)
@@ -566,6 +567,40 @@ def run_layout(args, w):
 
         step_bytes = sum(2 * x.numel() * 2 for x in xs)
         calls, kernel = 4, "sa_voxel_permute_kernel"
+    elif w.mode in ("bitmask", "blockmask"):
+        rows = w.B * w.H * w.G
+        dens = w.keep_pct / 100.0
+        if w.mode == "bitmask":
+            nw = -(-w.Nk // 32)
+            bits_ = torch.rand(rows, nw * 32, generator=g, device=dev) < dens
+            weights = (1 << torch.arange(32, device=dev, dtype=torch.int64))
+            mask = (bits_.view(rows, nw, 32).to(torch.int64) * weights).sum(-1).to(torch.int64)
+            mask = torch.where(mask >= (1 << 31), mask - (1 << 32), mask).to(torch.int32).contiguous()
+            nnz_est = int(bits_[:, :w.Nk].sum().item())
+            mask_bytes = mask.numel() * 4
+        else:
+            bk = 128
+            mask = (torch.rand(rows, -(-w.Nk // bk), generator=g, device=dev) < dens).to(torch.uint8)
+            nnz_est = int(mask.sum().item()) * bk
+            mask_bytes = mask.numel()
+        cap = rows * w.Nk
+        row_ptr = torch.empty(rows + 1, dtype=torch.int64, device=dev)
+        col = torch.empty(cap, dtype=torch.int32, device=dev)
+        p = sa.sa_problem(w.B, w.H, w.Nq, w.Nk, w.d, w.group, w.scale, 0)
+
+        def step():
+            if w.mode == "bitmask":
+                st = sa.lib.sparse_attn_index_from_bitmask(sa.ctypes.byref(p), sa._ptr(mask), sa._ptr(row_ptr),
+                                                           sa._ptr(col), cap, None, sa._stream(stream))
+            else:
+                st = sa.lib.sparse_attn_index_from_block_mask(sa.ctypes.byref(p), 128, sa._ptr(mask),
+                                                              sa._ptr(row_ptr), sa._ptr(col), cap, None,
+                                                              sa._stream(stream))
+            if st:
+                raise sa.SparseAttnError(st, "index from mask")
+
+        step_bytes = mask_bytes + 4 * nnz_est + 8 * (rows + 1)
+        calls, kernel = 3, "sa_fmt_emit_kernel"
     else:
         L = w.Nq  # one chunk: the newest 8 frames
         S = w.Nk // L
@@ -595,7 +630,7 @@ def run_layout(args, w):
         return
     pk, pk_kind = peaks()
     gbs = bytes_total / (ms_max * 1e-3) / 1e9
-    line = {"metric": "GB/s moved by the token-layout kernels (bytes read + written)", "value": gbs,
+    line = {"metric": "GB/s moved by the layout / index-format kernels (bytes read + written)", "value": gbs,
             "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
@@ -631,7 +666,7 @@ def main():
         run_reference(args, w)
     elif w.mode in ("cached", "colsum"):
         run_ours_dense(args, w)
-    elif w.mode in ("layout", "kvwindow"):
+    elif w.mode in ("layout", "kvwindow", "bitmask", "blockmask"):
         run_layout(args, w)
     else:
         run_ours(args, w)

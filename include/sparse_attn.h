@@ -267,6 +267,39 @@ sa_status sparse_attn_forward_delta(const sa_problem* problem, const void* q, co
                                     sa_stream_t stream);
 
 /*
+ * Index lists from other mask formats (the forward reads CSR).
+ *
+ * Bit-packed keep-mask (Chipmunk review, "Bitpacked Sparsity Masks": one bit
+ * per entry, 8x smaller than a byte mask): for each index row (unit b, h, g)
+ * ceil(Nk/32) uint32 words; key j is kept when bit (j % 32) of word j / 32
+ * is set (LSB first; the same bits as numpy.packbits(..., bitorder="little")
+ * of a row padded to a multiple of 32).  Bits past Nk are ignored.
+ *   mask_words  device uint32 [B*H*G, ceil(Nk/32)], 4-byte aligned
+ *
+ * Block-sparse mask (FG-Attn review, "The pith" and Fig. 6: masks of
+ * block-sparse attention methods feed the slice kernel directly): one byte
+ * per (index row, key block of block_k keys); non-zero keeps every key of the
+ * block (the last block holds Nk - (nb-1)*block_k keys).  Query blocks are
+ * the query groups of problem->group_size rows.
+ *   block_mask  device uint8 [B*H*G, ceil(Nk/block_k)]; block_k >= 1
+ *
+ * Both write ascending lists into col_idx with row_ptr as their offsets
+ * (rows may be empty).  row_ptr, col_idx, col_capacity, nnz_out_host:
+ * as for sparse_attn_build_index (nnz is data dependent: unless col_capacity
+ * >= B*H*G*Nk, nnz_out_host must be given; with it the call synchronises and
+ * returns SA_ERR_CAPACITY if the lists do not fit — rows that do not fit are
+ * not written).  Only problem's B, H, Nq, Nk, d and group_size are used.
+ */
+sa_status sparse_attn_index_from_bitmask(const sa_problem* problem, const uint32_t* mask_words,
+                                         int64_t* row_ptr, int32_t* col_idx, int64_t col_capacity,
+                                         int64_t* nnz_out_host, sa_stream_t stream);
+
+sa_status sparse_attn_index_from_block_mask(const sa_problem* problem, int32_t block_k,
+                                            const uint8_t* block_mask, int64_t* row_ptr,
+                                            int32_t* col_idx, int64_t col_capacity,
+                                            int64_t* nnz_out_host, sa_stream_t stream);
+
+/*
  * Token layout on either side of the attention path.
  *
  * Voxel reordering (Chipmunk review, "What carries the argument" / Alg. 1):

@@ -72,6 +72,11 @@ def _load():
     lib.sparse_attn_forward_delta.argtypes = [P(sa_problem), vp, vp, vp, vp, vp, i64, vp, vp,
                                               ctypes.c_float, vp, vp, vp]
     lib.sparse_attn_forward_delta.restype = ctypes.c_int
+    lib.sparse_attn_index_from_bitmask.argtypes = [P(sa_problem), vp, vp, vp, i64, P(ctypes.c_int64), vp]
+    lib.sparse_attn_index_from_bitmask.restype = ctypes.c_int
+    lib.sparse_attn_index_from_block_mask.argtypes = [P(sa_problem), ctypes.c_int32, vp, vp, vp, i64,
+                                                      P(ctypes.c_int64), vp]
+    lib.sparse_attn_index_from_block_mask.restype = ctypes.c_int
     lib.sparse_attn_voxel_permute.argtypes = [P(sa_voxel_grid), ctypes.c_int32, ctypes.c_int32, vp,
                                               vp, ctypes.c_int32, vp]
     lib.sparse_attn_voxel_permute.restype = ctypes.c_int
@@ -292,6 +297,47 @@ def sparse_attn_validate_index(row_ptr: torch.Tensor, col_idx: torch.Tensor, *, 
     return st
 
 
+def _from_mask(mask, B, H, Nq, Nk, d, group_size, block_k, col_capacity, stream):
+    p = sa_problem(B, H, Nq, Nk, d, group_size, 1.0 / math.sqrt(d), SA_OUT_BF16)
+    G = -(-Nq // group_size)
+    rows = B * H * G
+    dev = mask.device
+    row_ptr = torch.empty(rows + 1, dtype=torch.int64, device=dev)
+    cap = rows * Nk if col_capacity is None else int(col_capacity)
+    col_idx = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    nnz = ctypes.c_int64(0)
+    if block_k is None:
+        st = lib.sparse_attn_index_from_bitmask(ctypes.byref(p), _ptr(mask), _ptr(row_ptr),
+                                                _ptr(col_idx), cap, ctypes.byref(nnz), _stream(stream))
+        where = "sparse_attn_index_from_bitmask"
+    else:
+        st = lib.sparse_attn_index_from_block_mask(ctypes.byref(p), int(block_k), _ptr(mask),
+                                                   _ptr(row_ptr), _ptr(col_idx), cap,
+                                                   ctypes.byref(nnz), _stream(stream))
+        where = "sparse_attn_index_from_block_mask"
+    if st != SA_OK:
+        raise SparseAttnError(st, where)
+    return row_ptr, col_idx[:nnz.value], nnz.value
+
+
+def sparse_attn_index_from_bitmask(mask_words: torch.Tensor, *, B: int, H: int, Nq: int, Nk: int,
+                                   d: int = 128, group_size: int = 128,
+                                   col_capacity: int | None = None, stream=None):
+    """uint32 words [B*H*G, ceil(Nk/32)] (torch.int32 storage), key j = bit j%32
+    of word j//32 -> (row_ptr, col_idx, nnz).  Synchronises."""
+    _check(mask_words, torch.int32, "mask_words")
+    return _from_mask(mask_words, B, H, Nq, Nk, d, group_size, None, col_capacity, stream)
+
+
+def sparse_attn_index_from_block_mask(block_mask: torch.Tensor, block_k: int, *, B: int, H: int,
+                                      Nq: int, Nk: int, d: int = 128, group_size: int = 128,
+                                      col_capacity: int | None = None, stream=None):
+    """uint8 [B*H*G, ceil(Nk/block_k)] (non-zero = keep the key block) ->
+    (row_ptr, col_idx, nnz).  Synchronises."""
+    _check(block_mask, torch.uint8, "block_mask")
+    return _from_mask(block_mask, B, H, Nq, Nk, d, group_size, block_k, col_capacity, stream)
+
+
 def sparse_attn_voxel_permute(x: torch.Tensor, grid, voxel, *, inverse: bool = False,
                               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """x bf16 [B, H, N, d] (N = T*Hh*W) -> the same tokens in voxel order
@@ -338,4 +384,6 @@ forward = sparse_attn_forward
 forward_delta = sparse_attn_forward_delta
 validate_index = sparse_attn_validate_index
 voxel_permute = sparse_attn_voxel_permute
+index_from_bitmask = sparse_attn_index_from_bitmask
+index_from_block_mask = sparse_attn_index_from_block_mask
 kv_window_append = sparse_attn_kv_window_append

@@ -203,6 +203,49 @@ sa_status build_common(const sa_problem* p, const sa_select* sel, int32_t stat, 
   return SA_OK;
 }
 
+// Bit-packed (words) or block (blocks, block_k) masks to CSR.
+sa_status index_from_mask(const sa_problem* p, const uint32_t* words, const uint8_t* blocks,
+                          int32_t block_k, int64_t* row_ptr, int32_t* col_idx, int64_t col_capacity,
+                          int64_t* nnz_out_host, sa_stream_t stream) {
+  Dims dims;
+  sa_status st = check_problem(p, &dims);
+  if (st != SA_OK) return st;
+  if (!row_ptr || col_capacity < 0 || (col_capacity > 0 && !col_idx)) return SA_ERR_INVALID_ARG;
+  if (!aligned(row_ptr, 8) || (col_idx && !aligned(col_idx, 4)) || (words && !aligned(words, 4)))
+    return SA_ERR_INVALID_ARG;
+  if (blocks && block_k < 1) return SA_ERR_INVALID_ARG;
+  if (col_capacity < dims.rows * p->Nk && !nnz_out_host) return SA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_info(&sms)) != SA_OK) return st;
+  const int64_t W = words ? (int64_t(p->Nk) + 31) / 32 : (int64_t(p->Nk) + block_k - 1) / block_k;
+  const uint64_t mask_bytes = uint64_t(dims.rows) * uint64_t(W) * (words ? 4 : 1);
+  if (!in_device_allocation(words ? static_cast<const void*>(words) : static_cast<const void*>(blocks), mask_bytes) ||
+      !in_device_allocation(row_ptr, uint64_t(dims.rows + 1) * 8) ||
+      (col_capacity > 0 && !in_device_allocation(col_idx, uint64_t(col_capacity) * 4)))
+    return SA_ERR_INVALID_ARG;
+  sa::FmtArgs a;
+  a.words = words;
+  a.blocks = blocks;
+  a.row_ptr = row_ptr;
+  a.col_idx = col_idx;
+  a.rows = dims.rows;
+  a.capacity = col_capacity;
+  a.W = static_cast<int32_t>(W);
+  a.Nk = p->Nk;
+  a.block_k = words ? 32 : block_k;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = map_cuda(sa::launch_index_from_mask(a, sms, s))) != SA_OK) return st;
+  if (nnz_out_host) {
+    int64_t nnz = 0;
+    if (cudaMemcpyAsync(&nnz, row_ptr + dims.rows, 8, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return SA_ERR_CUDA;
+    *nnz_out_host = nnz;
+    if (nnz > col_capacity) return SA_ERR_CAPACITY;
+  }
+  return SA_OK;
+}
+
 // Argument checks and FwdArgs shared by the forward and the sparse delta.
 // row_ptr == col_idx == NULL: every unit keeps all keys (nnz ignored).
 sa_status forward_args(const sa_problem* p, const void* q, const void* k, const void* v,
@@ -309,6 +352,22 @@ sa_status sparse_attn_forward_delta(const sa_problem* p, const void* q, const vo
   a.base = base;
   a.sign = sign;
   return map_cuda(sa::launch_forward_delta(a, p->d, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sa_status sparse_attn_index_from_bitmask(const sa_problem* p, const uint32_t* mask_words,
+                                         int64_t* row_ptr, int32_t* col_idx, int64_t col_capacity,
+                                         int64_t* nnz_out_host, sa_stream_t stream) {
+  if (!mask_words) return SA_ERR_INVALID_ARG;
+  return index_from_mask(p, mask_words, nullptr, 0, row_ptr, col_idx, col_capacity, nnz_out_host, stream);
+}
+
+sa_status sparse_attn_index_from_block_mask(const sa_problem* p, int32_t block_k,
+                                            const uint8_t* block_mask, int64_t* row_ptr,
+                                            int32_t* col_idx, int64_t col_capacity,
+                                            int64_t* nnz_out_host, sa_stream_t stream) {
+  if (!block_mask) return SA_ERR_INVALID_ARG;
+  return index_from_mask(p, nullptr, block_mask, block_k, row_ptr, col_idx, col_capacity, nnz_out_host,
+                         stream);
 }
 
 sa_status sparse_attn_voxel_permute(const sa_voxel_grid* g, int32_t BH, int32_t d, const void* x,

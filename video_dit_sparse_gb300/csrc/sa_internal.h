@@ -92,6 +92,17 @@ struct KvArgs {
 };
 cudaError_t launch_kv_window(const KvArgs& a, int num_sms, cudaStream_t stream);
 
+// Bit-packed (words) or block (blocks) keep-masks to CSR lists.
+struct FmtArgs {
+  const uint32_t* words;   // [rows, W] or null
+  const uint8_t* blocks;   // [rows, W] or null
+  int64_t* row_ptr;
+  int32_t* col_idx;
+  int64_t rows, capacity;
+  int32_t W, Nk, block_k;
+};
+cudaError_t launch_index_from_mask(const FmtArgs& a, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_validate(const int64_t* row_ptr, const int32_t* col_idx, int64_t rows,
                             int64_t nnz, int32_t Nk, int32_t* status, cudaStream_t stream);
 

@@ -151,6 +151,15 @@ PRESETS["kvwindow_rollingkv"] = Workload("kvwindow_rollingkv", 1, 12, 128, 128, 
                                          (32, 22, 40), mode="kvwindow")
 
 
+# Mask-format conversions on the 69K grid, M = 128 (12960 index rows): a
+# bit-packed keep-mask with 20 % of the bits set, and a block mask of
+# 128-key blocks with 20 % kept.
+PRESETS["bitmask69k_top20"] = Workload("bitmask69k_top20", 1, 24, 128, 128, (18, 48, 80),
+                                       (18, 48, 80), mode="bitmask", keep_pct=20.0)
+PRESETS["blockmask69k_top20"] = Workload("blockmask69k_top20", 1, 24, 128, 128, (18, 48, 80),
+                                         (18, 48, 80), mode="blockmask", keep_pct=20.0)
+
+
 def preset(name: str) -> Workload:
     return PRESETS[name]
 
