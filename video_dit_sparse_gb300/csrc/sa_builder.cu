@@ -28,14 +28,6 @@ __device__ __forceinline__ float bf16_f(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// Monotone map float -> uint32 (larger score, larger key).
-__device__ __forceinline__ uint32_t order_key(float x) {
-  const uint32_t u = __float_as_uint(x);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
 
 template <typename T>
 __device__ __forceinline__ T warp_incl_scan(T v) {
@@ -779,6 +771,10 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
   uint32_t cut = 0;
   int32_t ties = 0;
   int64_t count = Nk;
+  // Every later phase reads this row (the sample, the bracket pass, the
+  // window's scores, the emission): start moving all of it into L2 now, so
+  // that those phases wait on L2 rather than DRAM latency.
+  for (int off = tid * 32; off < Nk; off += kSelThreads * 32) prefetch_l2(s + off);
 
   if (a.mode == SA_SELECT_THRESHOLD) {
     // keep p_j >= tau  <=>  sigma_j >= ln tau + max + ln Z
