@@ -736,23 +736,45 @@ __device__ void emit_row(const float* s, int Nk, uint32_t ck, int64_t nt, int64_
 __device__ __forceinline__ bool by_mass_mode(const SelArgs& a) { return a.mode != SA_SELECT_TOPK; }
 
 // Writes the indices of the set bits of kept[0, words) in ascending order to
-// col_idx[base, ...): each thread owns a run of words, the runs' offsets come
-// from one block scan of their popcounts.
+// col_idx[base, ...).  Warp w owns a contiguous run of words; the runs'
+// offsets come from one block scan of their popcounts.  A warp takes its run
+// 32 words at a time (lane = word): a warp scan of the popcounts places each
+// word's keys in the warp's staging buffer (1024 entries of shared memory),
+// and the pass leaves in coalesced stores.
 __device__ void emit_mask(const uint32_t* kept, int words, int64_t base, int32_t* col_idx,
-                          int64_t* scratch) {
-  const int per = (words + kSelThreads - 1) / kSelThreads;
-  const int w0 = min(words, static_cast<int>(threadIdx.x) * per), w1 = min(words, w0 + per);
+                          int64_t* scratch, int32_t* stage_all) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (words + kSelWarps - 1) / kSelWarps;
+  const int w0 = min(words, warp * per), w1 = min(words, w0 + per);
   int64_t n = 0;
-  for (int w = w0; w < w1; ++w) n += __popc(kept[w]);
+  for (int w = w0 + lane; w < w1; w += 32) n += __popc(kept[w]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+  // block scan over the warps' counts (only lane 0 of each warp contributes)
   int64_t total;
-  int64_t pos = base + block_excl_scan<int64_t>(n, &total, scratch);
-  for (int w = w0; w < w1; ++w) {
-    uint32_t bits = kept[w];
+  const int64_t before = block_excl_scan<int64_t>(lane == 0 ? n : 0, &total, scratch);
+  int64_t pos = base + __shfl_sync(0xffffffffu, before, 0);
+  int32_t* stage = stage_all + warp * 1024;
+  for (int wb = w0; wb < w1; wb += 32) {
+    const int w = wb + lane;
+    uint32_t bits = w < w1 ? kept[w] : 0u;
+    const int c = __popc(bits);
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    const int cnt = __shfl_sync(0xffffffffu, x, 31);
+    int off = x - c;
     while (bits) {
-      const int bit = __ffs(bits) - 1;
-      col_idx[pos++] = w * 32 + bit;
+      stage[off++] = w * 32 + (__ffs(bits) - 1);
       bits &= bits - 1;
     }
+    __syncwarp();
+    for (int i = lane; i < cnt; i += 32) col_idx[pos + i] = stage[i];
+    __syncwarp();
+    pos += cnt;
   }
 }
 
@@ -1056,7 +1078,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
             if (order_key(win_x ? wx[i] : s[j]) >= cut) atomicOr(&kept[j >> 5], 1u << (j & 31));
           }
           __syncthreads();
-          emit_mask(kept, a.mask_words, base, a.col_idx, sm.scan_c);
+          // the window's indices are no longer needed: its storage stages the lists
+          emit_mask(kept, a.mask_words, base, a.col_idx, sm.scan_c, sm.u.win.j);
         } else {
           emit_row(s, Nk, cut, ties, base, base + k, a.col_idx, sm.seg_sel, sm.seg_tie);
         }
