@@ -325,26 +325,26 @@ def run_ours(args, w):
     ms_max, units_total = aggregate(ms_step, float(flops), world)
     value = units_total / (ms_max * 1e-3) / 1e12
 
-    # end to end through the C ABI with host buffers
+    # end to end through the C ABI with host buffers: sparse_attn_layer_from_host
+    # overlaps the copies of one chunk of heads with the build + forward of
+    # the previous one (pinned host q, k, v in; o and lse out, every step)
     e2e_steps = max(3, min(args.steps, 20))
+    layer = sa.HostLayer(w.B, w.H, w.Nq, w.Nk, w.d, group_size=w.group, mode=w.mode, topk=w.topk,
+                         threshold=w.threshold, mass=w.mass, device=dev)
     h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    layer(hq, hk, hv, h_o, h_lse, stream=stream)  # warm-up
     torch.cuda.synchronize()
     e2e_ms = []
     for _ in range(e2e_steps):
         flush.zero_()
         e0.record(stream)
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        build()
-        fwd(nnz_now())
-        h_o.copy_(o, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        layer(hq, hk, hv, h_o, h_lse, stream=stream)
         e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
+    del layer
     e2e_ms_max, _ = aggregate(float(np.mean(e2e_ms)), 0.0, world)
     e2e_value = units_total / (e2e_ms_max * 1e-3) / 1e12
 

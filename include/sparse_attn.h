@@ -267,6 +267,47 @@ sa_status sparse_attn_forward_delta(const sa_problem* problem, const void* q, co
                                     sa_stream_t stream);
 
 /*
+ * One attention layer from host memory: copies overlapped with computation.
+ * (The pages describe no host interface; this is the runtime around the two
+ * calls above.)  The B*H (batch, head) pairs are split into chunks of
+ * consecutive heads: with more than two heads the first and the last chunk
+ * hold one head each (their copies are the ones computation cannot hide)
+ * and the heads between form chunks of heads_per_chunk (0: the middle split
+ * in three); at most 64 chunks.  For each chunk, on copy_in: Q, K, V from
+ * host to the device staging buffers; on compute, once they have landed:
+ * sparse_attn_build_index (this select, no synchronisation) and
+ * sparse_attn_forward; on copy_out, once that is done: O (and LSE) back to
+ * the host.  Chunk c+1 arrives and chunk c-1 leaves while chunk c computes.
+ * Every copy is one cudaMemcpyAsync of a contiguous range.  The call
+ * returns after enqueueing; the compute stream waits for the last copy, so
+ * synchronising `compute` completes the layer.  Copies of a call start only
+ * after the work an earlier call left on `compute`.
+ *   q_host, k_host, v_host   host bf16 [B,H,N,d]; pinned for the copies to overlap
+ *   o_host, lse_host         host outputs (o per problem->out_dtype; lse fp32
+ *                            [B,H,Nq], nullable together with lse_dev)
+ *   q_dev ... lse_dev        device staging of the same full shapes
+ *   row_ptr, col_idx, workspace
+ *                            device scratch for ONE chunk: row_ptr
+ *                            [heads_per_chunk*G + 1], col_idx of col_capacity
+ *                            >= heads_per_chunk*G*k (TOPK) or
+ *                            heads_per_chunk*G*Nk (else; SA_ERR_CAPACITY
+ *                            otherwise), workspace of the build's size for a
+ *                            problem of heads_per_chunk heads (0 stands for
+ *                            ceil((B*H - 2) / 3) when B*H > 2, else B*H)
+ *   compute, copy_in, copy_out   streams; a NULL copy stream means `compute`
+ * The lists are scratch (each chunk overwrites them).  Argument errors of
+ * the inner calls are returned as they are; nothing is allocated except the
+ * events that order the streams.
+ */
+sa_status sparse_attn_layer_from_host(const sa_problem* problem, const sa_select* select,
+                                      const void* q_host, const void* k_host, const void* v_host,
+                                      void* o_host, float* lse_host, void* q_dev, void* k_dev,
+                                      void* v_dev, void* o_dev, float* lse_dev, int64_t* row_ptr,
+                                      int32_t* col_idx, int64_t col_capacity, void* workspace,
+                                      size_t workspace_bytes, int32_t heads_per_chunk,
+                                      sa_stream_t compute, sa_stream_t copy_in, sa_stream_t copy_out);
+
+/*
  * Index lists from other mask formats (the forward reads CSR).
  *
  * Bit-packed keep-mask (Chipmunk review, "Bitpacked Sparsity Masks": one bit

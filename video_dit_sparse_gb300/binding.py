@@ -72,6 +72,10 @@ def _load():
     lib.sparse_attn_forward_delta.argtypes = [P(sa_problem), vp, vp, vp, vp, vp, i64, vp, vp,
                                               ctypes.c_float, vp, vp, vp]
     lib.sparse_attn_forward_delta.restype = ctypes.c_int
+    lib.sparse_attn_layer_from_host.argtypes = [P(sa_problem), P(sa_select), vp, vp, vp, vp, vp, vp,
+                                                vp, vp, vp, vp, vp, vp, i64, vp, ctypes.c_size_t,
+                                                ctypes.c_int32, vp, vp, vp]
+    lib.sparse_attn_layer_from_host.restype = ctypes.c_int
     lib.sparse_attn_index_from_bitmask.argtypes = [P(sa_problem), vp, vp, vp, i64, P(ctypes.c_int64), vp]
     lib.sparse_attn_index_from_bitmask.restype = ctypes.c_int
     lib.sparse_attn_index_from_block_mask.argtypes = [P(sa_problem), ctypes.c_int32, vp, vp, vp, i64,
@@ -375,6 +379,57 @@ def sparse_attn_kv_window_append(cache_k: torch.Tensor, cache_v: torch.Tensor,
     if st != SA_OK:
         raise SparseAttnError(st, "sparse_attn_kv_window_append")
     return int(valid.value)
+
+
+class HostLayer:
+    """One attention layer from pinned host tensors (sparse_attn_layer_from_host):
+    device staging, one chunk's scratch and two copy streams, allocated once
+    for a shape.  Calling it enqueues the copies in, the build + forward per
+    chunk of heads and the copies out; `synchronize()` waits for the layer."""
+
+    def __init__(self, B, H, Nq, Nk, d, *, group_size=128, mode="topk", topk=0, threshold=0.0,
+                 mass=0.99, heads_per_chunk=0, out_dtype=torch.bfloat16, with_lse=True,
+                 device=None):
+        dev = torch.device(device or "cuda")
+        self.p = sa_problem(B, H, Nq, Nk, d, group_size, 1.0 / math.sqrt(d), _OUT[out_dtype])
+        m = _MODES.get(mode, mode)
+        self.sel = sa_select(m, int(topk), float(threshold), float(mass))
+        BH = B * H
+        mid = BH - 2 if BH > 2 else 0
+        self.hc = heads_per_chunk if heads_per_chunk > 0 else (-(-mid // 3) if mid > 0 else BH)
+        self.hc = min(self.hc, BH)
+        G = -(-Nq // group_size)
+        kmax = min(max(int(topk), 1), Nk) if m == SA_SELECT_TOPK else Nk
+        cp = sa_problem(1, self.hc, Nq, Nk, d, group_size, self.p.scale, self.p.out_dtype)
+        self.ws = torch.empty(sparse_attn_build_index_workspace_size(cp), dtype=torch.uint8, device=dev)
+        self.row_ptr = torch.empty(self.hc * G + 1, dtype=torch.int64, device=dev)
+        self.cap = self.hc * G * kmax
+        self.col = torch.empty(self.cap, dtype=torch.int32, device=dev)
+        self.q = torch.empty(B, H, Nq, d, dtype=torch.bfloat16, device=dev)
+        self.k = torch.empty(B, H, Nk, d, dtype=torch.bfloat16, device=dev)
+        self.v = torch.empty_like(self.k)
+        self.o = torch.empty(B, H, Nq, d, dtype=out_dtype, device=dev)
+        self.lse = torch.empty(B, H, Nq, dtype=torch.float32, device=dev) if with_lse else None
+        self.copy_in = torch.cuda.Stream(device=dev)
+        self.copy_out = torch.cuda.Stream(device=dev)
+
+    def __call__(self, q_host, k_host, v_host, o_host, lse_host=None, stream=None):
+        for t in (q_host, k_host, v_host, o_host):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError("host tensors must be contiguous CPU tensors (pinned to overlap)")
+        if (lse_host is None) != (self.lse is None):
+            raise ValueError("lse_host must be given exactly when the layer keeps lse")
+        st = lib.sparse_attn_layer_from_host(
+            ctypes.byref(self.p), ctypes.byref(self.sel), _ptr(q_host), _ptr(k_host), _ptr(v_host),
+            _ptr(o_host), _ptr(lse_host), _ptr(self.q), _ptr(self.k), _ptr(self.v), _ptr(self.o),
+            _ptr(self.lse), _ptr(self.row_ptr), _ptr(self.col), self.cap, _ptr(self.ws),
+            self.ws.numel(), int(self.hc), _stream(stream), _stream(self.copy_in),
+            _stream(self.copy_out))
+        if st != SA_OK:
+            raise SparseAttnError(st, "sparse_attn_layer_from_host")
+
+    def synchronize(self, stream=None):
+        (stream if stream is not None else torch.cuda.current_stream()).synchronize()
 
 
 # Short aliases for Python callers.

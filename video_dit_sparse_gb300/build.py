@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsparse_attn.so")
-SOURCES = ["sa_api.cu", "sa_forward.cu", "sa_builder.cu", "sa_colstat.cu", "sa_layout.cu", "sa_format.cu", "sa_noalloc.cu"]
+SOURCES = ["sa_api.cu", "sa_forward.cu", "sa_builder.cu", "sa_colstat.cu", "sa_layout.cu", "sa_format.cu", "sa_pipeline.cu", "sa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

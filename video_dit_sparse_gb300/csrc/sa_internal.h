@@ -103,6 +103,9 @@ struct FmtArgs {
 };
 cudaError_t launch_index_from_mask(const FmtArgs& a, int num_sms, cudaStream_t stream);
 
+// sparse_attn_layer_from_host splits a layer into at most this many chunks.
+constexpr int kMaxPipelineChunks = 64;
+
 cudaError_t launch_validate(const int64_t* row_ptr, const int32_t* col_idx, int64_t rows,
                             int64_t nnz, int32_t Nk, int32_t* status, cudaStream_t stream);
 
