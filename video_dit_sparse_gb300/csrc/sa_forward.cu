@@ -30,6 +30,8 @@
 // division nothing cancels the rounding of P, so P goes to the PV MMA as two
 // bf16 terms (hi and the rounded remainder, in the two halves of the S
 // buffer) and O accumulates both products.
+#include <atomic>
+
 #include "sa_device.cuh"
 #include "sa_internal.h"
 #include "sa_tma.h"
@@ -580,6 +582,20 @@ static cudaError_t launch(const FwdArgs& a, const CUtensorMap& tmq, int num_sms,
   const int smem = C::kSmemBytes > 120 * 1024 ? C::kSmemBytes : 120 * 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  if (C::kRegSplit) {
+    // setmaxnreg.inc waits until the block's launch registers cover the new
+    // split; the compiler may launch with fewer than the maximum, so check
+    // the compiled count before any launch (never a block that could wait
+    // forever)
+    static std::atomic<int> regs_ok{0};  // 0 unknown, 1 enough, 2 too few (per instantiation)
+    if (regs_ok.load() == 0) {
+      cudaFuncAttributes attr;
+      if ((e = cudaFuncGetAttributes(&attr, kern)) != cudaSuccess) return e;
+      const long need = long(C::kRegSoftmax) * 4 * 32 + long(C::kRegOther) * (C::kThreads - 4 * 32);
+      regs_ok.store(long(attr.numRegs) * C::kThreads >= need ? 1 : 2);
+    }
+    if (regs_ok.load() != 1) return cudaErrorLaunchOutOfResources;
+  }
   const int64_t grid = a.units < num_sms ? a.units : num_sms;
   kern<<<static_cast<unsigned>(grid), C::kThreads, smem, stream>>>(a, tmq);
   return cudaGetLastError();
