@@ -70,7 +70,17 @@ struct FwdCfg {
   static constexpr int kQBytes = RB * kQBlock;
   static constexpr int kTile = BN * D * 2;       // one K or V tile
   static constexpr int kSCols = RB * BN;         // TMEM columns per S buffer
-  static constexpr int kOCol = 2 * kSCols;
+  // 128-row groups double-buffer S; with two row blocks each block has one S
+  // buffer (the MMA warp issues PV(j-1) of a block before QK(j) of the same
+  // block, so the tensor core, which runs one thread's MMAs in order, reads P
+  // before S is overwritten) and Q fits in TMEM: the QK MMAs then read only K
+  // from shared memory.
+  static constexpr int kSBufs = RB == 2 ? 1 : 2;
+  static constexpr int kOCol = kSBufs * kSCols;
+  static __device__ __forceinline__ uint32_t sbuf(uint32_t tt) { return kSBufs == 2 ? (tt & 1u) : 0u; }
+  static __device__ __forceinline__ uint32_t sphase(uint32_t tt) {
+    return kSBufs == 2 ? ((tt >> 1) & 1u) : (tt & 1u);
+  }
   // Q moves from shared memory into TMEM (D/2 columns per 128-row block) once
   // per unit, so the QK^T MMAs read only K from shared memory, when TMEM has
   // room for it.
@@ -243,9 +253,9 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         m = isfinite(lr0) ? lr0 * 1.4426950408889634f : INFINITY;
       }
       for (uint32_t j = 0; j < n; ++j) {
-        const uint32_t tt = t + j, b = tt & 1;
+        const uint32_t tt = t + j, b = C::sbuf(tt);
         const int nvalid = static_cast<int>(min64(BN, len - int64_t(j) * BN));
-        if (!mbar_wait(&bars->sfull[b][rb], (tt >> 1) & 1, abort)) goto done;
+        if (!mbar_wait(&bars->sfull[b][rb], C::sphase(tt), abort)) goto done;
         tc_fence_after();
         const uint32_t sbase = tmem + lane_base + b * C::kSCols + rb * BN;
         float x[BN];
@@ -281,7 +291,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         } else if (__any_sync(0xffffffffu, mx > m + C::kRescaleLog2)) {
           // O must hold PV of the previous tile before it is rescaled.
           const uint32_t tp = tt - 1;
-          if (!mbar_wait(&bars->pvdone[tp & 1][rb], (tp >> 1) & 1, abort)) goto done;
+          if (!mbar_wait(&bars->pvdone[C::sbuf(tp)][rb], C::sphase(tp), abort)) goto done;
           tc_fence_after();
           float alpha = 1.f;
           if (mx > m + C::kRescaleLog2) {
@@ -340,7 +350,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
       }
       {
         const uint32_t tl = t + n - 1;
-        if (!mbar_wait(&bars->pvdone[tl & 1][rb], (tl >> 1) & 1, abort)) goto done;
+        if (!mbar_wait(&bars->pvdone[C::sbuf(tl)][rb], C::sphase(tl), abort)) goto done;
         tc_fence_after();
         const float inv = DELTA ? a.sign : 1.f / lr;
         const uint32_t obase = tmem + lane_base + C::kOCol + rb * D;
@@ -374,31 +384,40 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
       const uint32_t v_lo = static_cast<uint32_t>(dv), v_hi = static_cast<uint32_t>(dv >> 32);
       uint32_t t = 0, un = 0;
       bool ok = true;
-      // O += P V for tile tt (first: overwrite O).
-      auto pv = [&](uint32_t tt, bool first) -> bool {
-        const uint32_t s = tt % STAGES, b = tt & 1;
-        if (!mbar_wait(&bars->vfull[s], (tt / STAGES) & 1, abort)) return false;
+      // V tile of tile tt has landed in shared memory.
+      auto v_ready = [&](uint32_t tt) -> bool {
+        if (!mbar_wait(&bars->vfull[tt % STAGES], (tt / STAGES) & 1, abort)) return false;
         fence_proxy_async_smem();  // V rows were written through the generic proxy
+        return true;
+      };
+      // O += P V of row block rb for tile tt (first: overwrite O).
+      auto pv_block = [&](uint32_t tt, int rb, bool first) -> bool {
+        const uint32_t s = tt % STAGES, b = C::sbuf(tt);
+        if (!mbar_wait(&bars->pfull[b][rb], C::sphase(tt), abort)) return false;
+        if (first && un > 0 && !mbar_wait(&bars->ofree[rb], (un - 1) & 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t a_tmem = tmem + b * C::kSCols + rb * BN;
+        const uint32_t d_tmem = tmem + C::kOCol + rb * D;
+        const uint32_t vs_lo = v_lo + ((s * C::kTile) >> 4);
 #pragma unroll
-        for (int rb = 0; rb < RB; ++rb) {
-          if (!mbar_wait(&bars->pfull[b][rb], (tt >> 1) & 1, abort)) return false;
-          if (first && un > 0 && !mbar_wait(&bars->ofree[rb], (un - 1) & 1, abort)) return false;
-          tc_fence_after();
-          const uint32_t a_tmem = tmem + b * C::kSCols + rb * BN;
-          const uint32_t d_tmem = tmem + C::kOCol + rb * D;
-          const uint32_t vs_lo = v_lo + ((s * C::kTile) >> 4);
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts_w(d_tmem, a_tmem + kk * 8, vs_lo + ((kk * 2048) >> 4), v_hi, kIdescPV,
+                   (!first || kk > 0) ? 1u : 0u);
+        if (DELTA) {  // the remainder of P, from the second half of the S buffer
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts_w(d_tmem, a_tmem + kk * 8, vs_lo + ((kk * 2048) >> 4), v_hi, kIdescPV,
-                     (!first || kk > 0) ? 1u : 0u);
-          if (DELTA) {  // the remainder of P, from the second half of the S buffer
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ts_w(d_tmem, a_tmem + BN / 2 + kk * 8, vs_lo + ((kk * 2048) >> 4), v_hi, kIdescPV, 1u);
-          }
-          mma_commit(&bars->pvdone[b][rb]);
+            mma_ts_w(d_tmem, a_tmem + BN / 2 + kk * 8, vs_lo + ((kk * 2048) >> 4), v_hi, kIdescPV, 1u);
         }
-        mma_commit(&bars->vempty[s]);
+        mma_commit(&bars->pvdone[b][rb]);
+        return true;
+      };
+      // O += P V for tile tt, every row block, then the V stage is free.
+      auto pv = [&](uint32_t tt, bool first) -> bool {
+        if (!v_ready(tt)) return false;
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb)
+          if (!pv_block(tt, rb, first)) return false;
+        mma_commit(&bars->vempty[tt % STAGES]);
         return true;
       };
       for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
@@ -420,13 +439,17 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           mma_commit(&bars->qempty);
         }
         for (uint32_t j = 0; j < n && ok; ++j) {
-          const uint32_t tt = t + j, s = tt % STAGES, b = tt & 1;
+          const uint32_t tt = t + j, s = tt % STAGES, b = C::sbuf(tt);
           if (!mbar_wait(&bars->kfull[s], (tt / STAGES) & 1, abort)) { ok = false; break; }
           fence_proxy_async_smem();  // K rows were written through the generic proxy
           tc_fence_after();
+          // one S buffer per block: PV(j-1) of a block goes before its QK(j)
+          const bool interleave = C::kSBufs == 1 && j >= 1;
+          if (interleave && !v_ready(tt - 1)) { ok = false; break; }
           const uint32_t ks_lo = k_lo + ((s * C::kTile) >> 4);
 #pragma unroll
           for (int rb = 0; rb < RB; ++rb) {
+            if (interleave && !pv_block(tt - 1, rb, j == 1)) { ok = false; break; }
             const uint32_t d_tmem = tmem + b * C::kSCols + rb * BN;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -440,9 +463,11 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
             }
             mma_commit(&bars->sfull[b][rb]);
           }
+          if (!ok) break;
+          if (interleave) mma_commit(&bars->vempty[(tt - 1) % STAGES]);
           mma_commit(&bars->kempty[s]);
           if (!C::kQTmem && j == n - 1) mma_commit(&bars->qempty);
-          if (j >= 1 && !pv(tt - 1, j == 1)) ok = false;
+          if (C::kSBufs == 2 && j >= 1 && !pv(tt - 1, j == 1)) ok = false;
         }
         if (ok && !pv(t + n - 1, n == 1)) ok = false;
         t += n;
