@@ -37,17 +37,25 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_FLUSH_BYTES = 512 << 20
 
 
-def kernels_per_step(mode: str) -> int:
-    """Our kernels per step: mean query, scores, select, scan, [emit,] forward.
-    TOPK lists are written by the select kernel; the other modes add the
-    emit kernel once the row offsets are known.  Dense-step workloads: dense
-    forward, column statistics, select, scan, [emit,] and the sparse forward
-    (cached mask) or the two sparse deltas (column sums, TOPK)."""
+def kernels_per_step(mode: str, topk: int = 0, Nk: int = 0) -> int:
+    """Our kernels per step.  TOPK by mean query over at least 8192 keys (a
+    multiple of 8): mean query, sample scores, bracket, classifying scores,
+    finalize, the score and select kernels on the rows it left (usually
+    none), scan, forward; keeping every key: finalize, scan, forward.  Other
+    selections: mean query, scores, select, scan, [emit,] forward (TOPK lists
+    are written by the select kernel; the other modes add the emit kernel
+    once the row offsets are known).  Dense-step workloads: dense forward,
+    column statistics, select, scan, [emit,] and the sparse forward (cached
+    mask) or the two sparse deltas (column sums, TOPK)."""
     if mode == "cached":
         return 6
     if mode == "colsum":
         return 6
-    return 5 if mode == "topk" else 6
+    if mode == "topk":
+        if topk >= Nk:
+            return 3
+        return 9 if Nk >= 8192 and Nk % 8 == 0 else 5
+    return 6
 
 
 def peaks():
@@ -363,7 +371,7 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": workload_config(w, pairs),
             "ms_build_index": float(np.mean(t_build)), "ms_forward": fwd_ms,
-            "gpu_launches": kernels_per_step(w.mode) * args.steps,
+            "gpu_launches": kernels_per_step(w.mode, w.topk, w.Nk) * args.steps,
             "roofline": roofline,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": int(3 * q.numel() * 2),

@@ -91,3 +91,111 @@ def test_builder_repeatable():
     a = gpu_build(q, k, 128, "mass", mass=0.95)
     b = gpu_build(q, k, 128, "mass", mass=0.95)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------- TOPK over >= 8192 keys
+# These lists come from the path without a score matrix: sampled scores, a
+# bracket around each row's cut, one classifying score pass, the exact cut
+# among the bracketed candidates.  Rows it cannot bracket are selected from
+# their full scores afterwards; `fallback_rows` reads how many there were
+# (the int32 at the start of the workspace's last region: count, row list,
+# unit flags), or -1 when the path was not taken (the workspace starts as
+# 0xFF bytes and only that path clears the count).
+def _workspace(qd, kd, M):
+    from video_dit_sparse_gb300 import binding as sa
+    ws = torch.full((sa.sparse_attn_build_index_workspace_size(sa.problem(qd, kd, M)),), 255,
+                    dtype=torch.uint8, device="cuda")
+    B, H, Nq, _ = qd.shape
+    rows = B * H * (-(-Nq // M))
+    return ws, ws.numel() - ((256 + 8 * rows + 255) // 256) * 256
+
+
+def fallback_rows(ws, off):
+    return int(ws[off:off + 4].view(torch.int32).item())
+
+
+def build_topk(q, k, M, topk):
+    from video_dit_sparse_gb300 import binding as sa
+    qd, kd = P.to_dev(q), P.to_dev(k)
+    ws, off = _workspace(qd, kd, M)
+    rp, col, nnz = sa.sparse_attn_build_index(qd, kd, "topk", topk=topk, group_size=M, workspace=ws)
+    torch.cuda.synchronize()
+    return rp, col, nnz, fallback_rows(ws, off)
+
+
+def check_topk(q, k, M, topk, rp, col):
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    rows = B * H * (-(-Nq // M))
+    ref_lists, ref_cut, ref_sc = oracle.build_index(q, k, M, 1.0 / math.sqrt(d), "topk", topk=topk)
+    rpn = rp.cpu().numpy()
+    assert np.all(np.diff(rpn) == min(topk, Nk)) and rpn[-1] == rows * min(topk, Nk)
+    P.compare_lists(rp, col, range(rows), ref_lists, ref_cut, ref_sc, Nk)
+
+
+DIRECT_CASES = [
+    # (d, M, grid_q, grid_k, topk): ragged 128-row chunks of groups (G = 150),
+    # d = 64, 192-row groups, a top key, nearly every key, every key
+    (128, 128, (12, 40, 40), (10, 25, 40), 1500),
+    (64, 128, (4, 16, 16), (16, 32, 32), 3277),
+    (128, 192, (6, 16, 16), (10, 25, 40), 1000),
+    (128, 128, (4, 16, 16), (8, 32, 32), 1),
+    (128, 128, (4, 16, 16), (8, 32, 32), 8191),
+    (128, 128, (4, 16, 16), (8, 32, 32), 8192),
+]
+
+
+@pytest.mark.parametrize("d,M,grid_q,grid_k,topk", DIRECT_CASES)
+def test_topk_direct_matches_oracle(d, M, grid_q, grid_k, topk):
+    q, k, _ = field(1, 2, d, grid_q, grid_k, seed=topk + d)
+    rp, col, nnz, nf = build_topk(q, k, M, topk)
+    check_topk(q, k, M, topk, rp, col)
+    if topk < k.shape[2]:
+        assert nf == 0  # field inputs: every row bracketed
+
+
+def test_topk_direct_identical_keys_fall_back():
+    # every score of a row ties: the bracket holds the whole row, more than
+    # the finalize takes, so every row goes through the full-score selection
+    # (lowest indices first among equal scores)
+    q, k, _ = field(1, 2, 128, (4, 16, 16), (8, 32, 32), seed=5)
+    k = np.ascontiguousarray(np.broadcast_to(k[:, :, :1], k.shape))
+    rp, col, nnz, nf = build_topk(q, k, 128, 1000)
+    rows = 2 * 8
+    assert nf == rows
+    check_topk(q, k, 128, 1000, rp, col)
+    first = np.arange(1000, dtype=np.int32)
+    c = col.cpu().numpy().reshape(rows, 1000)
+    assert all(np.array_equal(c[r], first) for r in range(rows))
+
+
+def _tall_keys(grid_k, seed, every):
+    # every `every`-th key is all ones and the queries are offset by +3:
+    # those keys tie far above every other key
+    q, k, _ = field(1, 1, 128, (4, 16, 16), grid_k, seed=seed)
+    one = np.uint16(np.float32(1.0).view(np.uint32) >> 16)
+    qf = (q.astype(np.uint32) << 16).view(np.float32) + np.float32(3.0)
+    q = (qf.view(np.uint32) >> 16).astype(np.uint16)  # truncated to bf16: any bits are inputs
+    k = k.copy()
+    k[:, :, ::every, :] = one
+    return q, k
+
+
+def test_topk_direct_unrepresentative_sample_falls_back():
+    # the sampled keys (every 8th) are the tied ones: the bracket sits among
+    # them and holds fewer than k keys, so every row falls back
+    q, k = _tall_keys((16, 32, 32), seed=6, every=8)
+    rp, col, nnz, nf = build_topk(q, k, 128, 3277)
+    assert nf == 8
+    check_topk(q, k, 128, 3277, rp, col)
+
+
+def test_topk_direct_ties_at_the_cut_by_index():
+    # k below the 512 tied keys: the cut falls among equal scores and the
+    # lowest indices are kept
+    q, k = _tall_keys((8, 32, 32), seed=7, every=16)
+    rp, col, nnz, nf = build_topk(q, k, 128, 500)
+    assert nf == 0
+    check_topk(q, k, 128, 500, rp, col)
+    c = col.cpu().numpy().reshape(8, 500)
+    assert all(np.array_equal(c[r], np.arange(0, 8000, 16)) for r in range(8))

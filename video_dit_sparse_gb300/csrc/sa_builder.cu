@@ -106,7 +106,13 @@ struct ScoreArgs {
   int32_t Nk, gchunks, ksplit, tiles_per_split, ntiles;
   float scale;
   int32_t* status;
+  // score only the (head, 128-row chunk) units flagged non-zero here
+  const int32_t* unit_filter = nullptr;
 };
+
+__device__ __forceinline__ bool skip_unit(const ScoreArgs& a, int64_t bh, int gc) {
+  return a.unit_filter && a.unit_filter[bh * a.gchunks + gc] == 0;
+}
 
 template <int D>
 struct ScoreCfg {
@@ -191,6 +197,7 @@ __global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1)
       int64_t bh;
       int gc, t0, t1;
       score_unit(a, u, &bh, &gc, &t0, &t1);
+      if (skip_unit(a, bh, gc)) continue;
       for (int tile = t0; tile < t1; ++tile, ++t) {
         const uint32_t b = t & 1;
         if (!mbar_wait(&bars->dfull[b], (t >> 1) & 1, abort)) goto done;
@@ -226,7 +233,7 @@ __global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1)
         int64_t bh;
         int gc, t0, t1;
         score_unit(a, u, &bh, &gc, &t0, &t1);
-        if (t1 <= t0) continue;
+        if (t1 <= t0 || skip_unit(a, bh, gc)) continue;
         if (!mbar_wait(&bars->qfull, un & 1, abort)) break;
         for (int tile = t0; tile < t1; ++tile, ++t) {
           const uint32_t s = t % S, b = t & 1;
@@ -268,7 +275,7 @@ __global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1)
       int64_t bh;
       int gc, t0, t1;
       score_unit(a, u, &bh, &gc, &t0, &t1);
-      if (t1 <= t0) continue;
+      if (t1 <= t0 || skip_unit(a, bh, gc)) continue;
       if (un > 0 && !mbar_wait(&bars->qempty, (un - 1) & 1, abort)) goto done;
       // mean-query rows bh*G + g0 .. +127 (rows of the next head or past the
       // end only feed columns that are never written)
@@ -283,10 +290,10 @@ __global__ void __launch_bounds__(ScoreCfg<D>::kThreads, 1)
         const uint32_t s = t % S;
         if (!mbar_wait(&bars->kempty[s], ((t / S) & 1) ^ 1, abort)) goto done;
         mbar_expect_tx(&bars->kfull[s], C::kTile);
-        const int krow = static_cast<int>(bh * a.Nk + int64_t(tile) * 128);
 #pragma unroll
         for (int cb = 0; cb < D / 64; ++cb)
-          tma_load_2d(kb + s * C::kTile + cb * 128 * 128, &tm_k, 64 * cb, krow, &bars->kfull[s]);
+          tma_load_3d(kb + s * C::kTile + cb * 128 * 128, &tm_k, 64 * cb, tile * 128, static_cast<int>(bh),
+                      &bars->kfull[s]);
       }
       ++un;
     }
@@ -319,6 +326,8 @@ struct SelArgs {
   int64_t col_capacity;
   int32_t mask_words;    // TOPK: words of the kept-key bitmask (0: emit by re-reading the row)
   int32_t level;         // THRESHOLD compares the score itself with ln(threshold)
+  const int32_t* row_list = nullptr;   // select only these rows (count in *row_count)
+  const int32_t* row_count = nullptr;
 };
 
 constexpr int kSelThreads = 256;            // one row per block, 4 blocks resident per SM
@@ -778,15 +787,12 @@ __device__ void emit_mask(const uint32_t* kept, int words, int64_t base, int32_t
   }
 }
 
-__global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs a) {
-  extern __shared__ uint8_t sel_raw[];
-  SelSmem& sm = *reinterpret_cast<SelSmem*>(sel_raw);
-  // TOPK: bit j of kept[j / 32] marks key j as kept (keys above the bracket
-  // during the window pass, kept keys of the window after the selection).
-  uint32_t* kept = reinterpret_cast<uint32_t*>(sel_raw + sizeof(SelSmem));
+// The selection of one score row by the whole block.  TOPK: bit j of
+// kept[j / 32] marks key j as kept (keys above the bracket during the window
+// pass, kept keys of the window after the selection).
+__device__ void select_row(const SelArgs& a, const int64_t row, SelSmem& sm, uint32_t* kept) {
   const bool use_mask = !by_mass_mode(a) && a.col_idx && a.mask_words > 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t row = blockIdx.x;
   const float* s = a.scores + row * a.ld;
   const int Nk = a.Nk;
   const bool by_mass = a.mode == SA_SELECT_MASS;
@@ -1093,6 +1099,25 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs
   }
 }
 
+// One row per block, or (row_list set) the listed rows only: the rows that
+// the TOPK path without a score matrix could not bracket, whose scores the
+// score kernel has written for this kernel.
+template <bool LIST>
+__global__ void __launch_bounds__(kSelThreads, 4) sa_select_kernel(const SelArgs a) {
+  extern __shared__ uint8_t sel_raw[];
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(sel_raw);
+  uint32_t* kept = reinterpret_cast<uint32_t*>(sel_raw + sizeof(SelSmem));
+  if (!LIST) {
+    select_row(a, blockIdx.x, sm, kept);
+    return;
+  }
+  const int n = *a.row_count;
+  for (int i = blockIdx.x; i < n; i += gridDim.x) {
+    select_row(a, a.row_list[i], sm, kept);
+    __syncthreads();
+  }
+}
+
 // ------------------------------------------------------------ 4. scan
 __global__ void __launch_bounds__(1024) sa_scan_kernel(const int64_t* counts, int64_t rows,
                                                        int64_t* row_ptr, int64_t* nnz,
@@ -1127,6 +1152,673 @@ __global__ void __launch_bounds__(kSelThreads) sa_emit_kernel(const float* score
   const int64_t base = row_ptr[row], end = row_ptr[row + 1];
   if (end > capacity) return;  // reported by the scan
   emit_row(scores + row * ld, Nk, cut[row], ties[row], base, end, col_idx, seg_sel, seg_tie);
+}
+
+// ------------------------------------------------------------ 6. TOPK without a score matrix
+// TOPK lists need each row's k-th largest score and the keys above it, not the
+// scores themselves, so the fp32 score matrix (rows x Nk, written once and read
+// several times by the select kernel) is replaced by three passes:
+//   sa_score_kernel<D>            scores of every stride-th key (a strided TMA
+//                                 map over K) into a small sample matrix;
+//   sa_bracket_kernel             per row, two score values lo <= hi around the
+//                                 cut: the sample's order statistics at the
+//                                 expected rank of the cut -/+ four binomial
+//                                 standard deviations;
+//   sa_rowscore_kernel<D>         every score, classified as it leaves TMEM:
+//                                 above hi -> a bit of the row's keep-mask, in
+//                                 [lo, hi] -> an (index, score) candidate;
+//   sa_topk_finalize_kernel       the exact cut among the candidates (the
+//                                 select kernel's histogram descent), their
+//                                 bits, and ascending emission from the mask.
+// The score MMA here puts the mean queries on TMEM lanes (A = 128 groups x d,
+// B = 128 keys x d), so a thread owns one row and builds its mask words and
+// candidate list without any exchange.  A row whose bracket misses the cut or
+// overflows its candidate storage is listed; the score kernel then writes the
+// fp32 scores of the listed rows' units and the select kernel selects those
+// rows, so the lists are exact in every case.
+// Key split ks of a unit takes the key tiles ks, ks + ksplit, ... (spread
+// over the whole sequence, so that every split sees about the same share of
+// a row's candidates however they cluster); each (row, split, half of the
+// tile's columns) has its own candidate region of `cap` slots.
+struct RowScoreArgs {
+  int64_t G, units;
+  int32_t Nk, gchunks, ksplit, ntiles;
+  float scale;
+  const float2* lohi;   // (lo, hi) per row
+  uint32_t* mask;       // [rows, ld_mask] words, bit j mod 32 of word j / 32: key j above hi
+  int64_t ld_mask;
+  uint2* cand;          // [rows, 2 * ksplit regions, cap]: (key, score bits)
+  int32_t cap;
+  int32_t* nabove;      // [rows, 2 * ksplit]: keys above hi
+  int32_t* ncand;       // [rows, 2 * ksplit]: keys in [lo, hi] (may exceed cap)
+  int32_t* status;
+};
+
+template <int D>
+struct RowScoreCfg {
+  static constexpr int kStages = 3;
+  static constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, 64 key columns each
+  static constexpr int kMmaWarp = kEpiWarps, kTmaWarp = kEpiWarps + 1;
+  static constexpr int kThreads = 32 * (kEpiWarps + 2);
+  static constexpr int kTile = 128 * D * 2;  // 128 rows of d bf16
+  // each epilogue warp stages its 32 rows x 64 raw scores, [c / 4][lane] float4s
+  static constexpr int kStage = 32 * 64 * 4;
+  static constexpr int kSmemBytes = 1024 + 2 * kTile + kStages * kTile + kEpiWarps * kStage + 1024;
+  static constexpr int kTmemCols = 256;      // two 128-column accumulators
+};
+
+__device__ __forceinline__ void rs_unit(const RowScoreArgs& a, int64_t u, int64_t* bh, int* gc,
+                                        int* ks) {
+  const int64_t per_bh = int64_t(a.gchunks) * a.ksplit;
+  *bh = u / per_bh;
+  const int rem = static_cast<int>(u % per_bh);
+  *gc = rem / a.ksplit;
+  *ks = rem % a.ksplit;
+}
+
+// For s > 0: the largest x with fl(x * s) <= hi (+inf for hi = +inf), and
+// the smallest x with fl(x * s) >= lo (-inf for lo = -inf); rounding is
+// monotone in x, so a few ulp steps from the quotient find them.  A zero
+// result is returned as +0 (floor) or -0 (ceil), so that the sign of
+// floor - x and of x - ceil is that of the comparison.
+__device__ __forceinline__ float score_floor(float hi, float s) {
+  if (!(hi < INFINITY)) return INFINITY;
+  float x = hi / s;
+  for (int i = 0; i < 8 && x * s > hi; ++i) x = nextafterf(x, -INFINITY);
+  for (int i = 0; i < 8 && nextafterf(x, INFINITY) * s <= hi; ++i) x = nextafterf(x, INFINITY);
+  return x == 0.f ? 0.f : x;
+}
+__device__ __forceinline__ float score_ceil(float lo, float s) {
+  if (!(lo > -INFINITY)) return -INFINITY;
+  float x = lo / s;
+  for (int i = 0; i < 8 && x * s < lo; ++i) x = nextafterf(x, INFINITY);
+  for (int i = 0; i < 8 && nextafterf(x, -INFINITY) * s >= lo; ++i) x = nextafterf(x, -INFINITY);
+  return x == 0.f ? -0.f : x;
+}
+
+template <int D>
+__global__ void __launch_bounds__(RowScoreCfg<D>::kThreads, 1)
+    sa_rowscore_kernel(const RowScoreArgs a, const __grid_constant__ CUtensorMap tm_qhi,
+                       const __grid_constant__ CUtensorMap tm_qlo,
+                       const __grid_constant__ CUtensorMap tm_k) {
+  using C = RowScoreCfg<D>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sQh = smem;
+  uint8_t* sQl = sQh + C::kTile;
+  uint8_t* sK = sQl + C::kTile;
+  uint8_t* sStage = sK + S * C::kTile;
+  ScoreBars* bars = reinterpret_cast<ScoreBars*>(sStage + C::kEpiWarps * C::kStage);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&bars->kfull[s], 1);
+      mbar_init(&bars->kempty[s], 1);
+    }
+    mbar_init(&bars->qfull, 1);
+    mbar_init(&bars->qempty, 1);
+    mbar_init(&bars->drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->dfull[b], 1);
+      mbar_init(&bars->dempty[b], C::kEpiWarps);  // one arrival per epilogue warp
+    }
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp < C::kEpiWarps) {
+    // ------------------------------------------------------------ epilogue
+    // Thread = one mean-query row (TMEM lane), 64 key columns of each tile.
+    const int quarter = warp & 3, half = warp >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int gi = quarter * 32 + lane;
+    uint32_t t = 0;
+    for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
+      int64_t bh;
+      int gc, ks;
+      rs_unit(a, u, &bh, &gc, &ks);
+      const int64_t g = int64_t(gc) * 128 + gi;
+      const bool valid = g < a.G;
+      const int64_t row = bh * a.G + g;
+      const int64_t region = (row * a.ksplit + ks) * 2 + half;
+      // scale > 0: scale*x > hi <=> x > xa and scale*x < lo <=> x < xb, with
+      // xa the largest x whose rounded score is <= hi, xb the smallest whose
+      // rounded score is >= lo (found from the quotients by stepping ulps)
+      float xa = 0.f, xb = 0.f;
+      if (valid) {
+        const float2 b = a.lohi[row];
+        xa = score_floor(b.y, a.scale);
+        xb = score_ceil(b.x, a.scale);
+      }
+      uint2* cbase = a.cand + region * a.cap;
+      const int cap = a.cap;
+      int nab = 0, nc = 0;
+      for (int tile = ks; tile < a.ntiles; tile += a.ksplit, ++t) {
+        const uint32_t b = t & 1;
+        // (the whole warp leaves together: the steps below are warp-collective)
+        const bool got = mbar_wait(&bars->dfull[b], (t >> 1) & 1, abort);
+        if (!__all_sync(0xffffffffu, got)) goto done;
+        tc_fence_after();
+        float x[64];
+        const uint32_t src = tmem + lane_base + b * 128 + half * 64;
+        tmem_ld32(src, reinterpret_cast<uint32_t*>(x));
+        tmem_ld32(src + 32, reinterpret_cast<uint32_t*>(x + 32));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->dempty[b]);
+        // (rows past G take part in the warp's collective steps with no keys)
+        const int j0 = tile * 128 + half * 64;
+        // key c is above when xa - x < 0 and below when x - xb < 0 (for floats
+        // p != q, p - q is never zero; xa is never -0 and xb never +0): the
+        // sign bits are funnel-shifted into words, highest key first, in
+        // four chains of 16 keys per word
+        uint32_t w[2], bl[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a0 = 0u, a1 = 0u, b0 = 0u, b1 = 0u;
+#pragma unroll
+          for (int c = 15; c >= 0; --c) {
+            a0 = shl_in(a0, __float_as_uint(xa - x[32 * h + c]));
+            a1 = shl_in(a1, __float_as_uint(xa - x[32 * h + 16 + c]));
+            b0 = shl_in(b0, __float_as_uint(x[32 * h + c] - xb));
+            b1 = shl_in(b1, __float_as_uint(x[32 * h + 16 + c] - xb));
+          }
+          w[h] = (a1 << 16) | a0;
+          bl[h] = (b1 << 16) | b0;
+        }
+        uint32_t cw[2] = {~(w[0] | bl[0]), ~(w[1] | bl[1])};  // neither above nor below
+        if (j0 + 64 > a.Nk || !valid) {
+          const int rem = valid ? a.Nk - j0 : 0;  // keys of this half that exist
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int r = rem - 32 * h;
+            const uint32_t keep = r >= 32 ? 0xFFFFFFFFu : (r <= 0 ? 0u : (1u << r) - 1u);
+            w[h] &= keep;
+            cw[h] &= keep;
+          }
+        }
+        if (valid) {
+          nab += __popc(w[0]) + __popc(w[1]);
+          *reinterpret_cast<uint2*>(a.mask + row * a.ld_mask + (j0 >> 5)) = make_uint2(w[0], w[1]);
+        }
+        // the candidates' scores leave through the warp's staging area, each
+        // lane walking its own candidate bits
+        if (__any_sync(0xffffffffu, (cw[0] | cw[1]) != 0u)) {
+          float4* st4 = reinterpret_cast<float4*>(sStage + warp * C::kStage);
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4)
+            st4[c4 * 32 + lane] = make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
+          __syncwarp();
+          const float* st = reinterpret_cast<const float*>(st4);
+          uint64_t cm = (static_cast<uint64_t>(cw[1]) << 32) | cw[0];
+          while (cm) {
+            const int c = __ffsll(static_cast<long long>(cm)) - 1;
+            cm &= cm - 1;
+            if (nc < cap)
+              cbase[nc] = make_uint2(static_cast<uint32_t>(j0 + c),
+                                     __float_as_uint(st[((c >> 2) * 32 + lane) * 4 + (c & 3)] * a.scale));
+            ++nc;
+          }
+          __syncwarp();
+        }
+      }
+      if (valid) {
+        a.nabove[region] = nab;
+        a.ncand[region] = nc;
+      }
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = idesc_bf16(128, 128, false, false);
+      const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl), kb = smem_u32(sK);
+      uint32_t t = 0, un = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        int64_t bh;
+        int gc, ks;
+        rs_unit(a, u, &bh, &gc, &ks);
+        if (ks >= a.ntiles) continue;
+        if (!mbar_wait(&bars->qfull, un & 1, abort)) break;
+        for (int tile = ks; tile < a.ntiles; tile += a.ksplit, ++t) {
+          const uint32_t s = t % S, b = t & 1;
+          if (!mbar_wait(&bars->kfull[s], (t / S) & 1, abort) ||
+              !mbar_wait(&bars->dempty[b], ((t >> 1) & 1) ^ 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + b * 128;
+          // D[group][key] = q_hi . k, then += q_lo . k
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
+            mma_ss(d_tmem, sw128_desc(qh + off, 16, 1024), sw128_desc(kb + s * C::kTile + off, 16, 1024),
+                   kIdesc, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 128 * 128 + (kk & 3) * 32;
+            mma_ss(d_tmem, sw128_desc(ql + off, 16, 1024), sw128_desc(kb + s * C::kTile + off, 16, 1024),
+                   kIdesc, 1u);
+          }
+          mma_commit(&bars->dfull[b]);
+          mma_commit(&bars->kempty[s]);
+          if (tile + a.ksplit >= a.ntiles) mma_commit(&bars->qempty);
+        }
+        ++un;
+      }
+      mma_commit(&bars->drain);
+      const long long c0 = clock64();
+      while (!mbar_test(&bars->drain, 0) && clock64() - c0 < kWaitLimitCycles) {
+      }
+    }
+  } else if (lane == 0) {
+    // ------------------------------------------------------------ loads (TMA)
+    const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl), kb = smem_u32(sK);
+    uint32_t t = 0, un = 0;
+    for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
+      int64_t bh;
+      int gc, ks;
+      rs_unit(a, u, &bh, &gc, &ks);
+      if (ks >= a.ntiles) continue;
+      if (un > 0 && !mbar_wait(&bars->qempty, (un - 1) & 1, abort)) goto done;
+      // mean-query rows bh*G + gc*128 .. +127 (rows past the head only feed
+      // rows that are never written)
+      const int qrow = static_cast<int>(bh * a.G + int64_t(gc) * 128);
+      mbar_expect_tx(&bars->qfull, 2 * C::kTile);
+#pragma unroll
+      for (int cb = 0; cb < D / 64; ++cb) {
+        tma_load_2d(qh + cb * 128 * 128, &tm_qhi, 64 * cb, qrow, &bars->qfull);
+        tma_load_2d(ql + cb * 128 * 128, &tm_qlo, 64 * cb, qrow, &bars->qfull);
+      }
+      for (int tile = ks; tile < a.ntiles; tile += a.ksplit, ++t) {
+        const uint32_t s = t % S;
+        if (!mbar_wait(&bars->kempty[s], ((t / S) & 1) ^ 1, abort)) goto done;
+        mbar_expect_tx(&bars->kfull[s], C::kTile);
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb)
+          tma_load_3d(kb + s * C::kTile + cb * 128 * 128, &tm_k, 64 * cb, tile * 128, static_cast<int>(bh),
+                      &bars->kfull[s]);
+      }
+      ++un;
+    }
+  }
+done:
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && bars->abort) report(a.status, SA_DEVERR_TIMEOUT);
+  if (warp == C::kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// Per row (one warp each): lo <= hi around the cut from the row's samples.
+// The samples are spread over kBrBins linear bins between the minimum and
+// maximum of the first 1024 of them, widened by an eighth (samples outside go
+// to the end bins, whose outer edges count as -inf and inf); hi is the upper
+// edge of the bin
+// holding sample rank r_hi (counted from the top, 0-based) and lo the lower
+// edge of the bin holding rank r_lo, so at most r_hi samples lie above hi and
+// more than r_lo at or above lo.  A non-finite estimate gives (-inf, inf):
+// every key a candidate.
+constexpr int kBrBins = 1024;
+constexpr int kBrWarps = 4;
+__global__ void __launch_bounds__(32 * kBrWarps) sa_bracket_kernel(const float* samp, int64_t ld_samp,
+                                                                    int32_t S, int64_t rows, float r_hi,
+                                                                    float r_lo, float2* lohi) {
+  __shared__ uint32_t hist_all[kBrWarps][kBrBins];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t row = int64_t(blockIdx.x) * kBrWarps + warp;
+  if (row >= rows) return;  // warps are independent: no block barrier below
+  uint32_t* hist = hist_all[warp];
+  const float* x = samp + row * ld_samp;
+  const float nan = __int_as_float(0x7fffffff);
+  float mn = INFINITY, mx = -INFINITY;
+  {
+    const int ne = S < 1024 ? S : 1024;
+    float v[32];
+#pragma unroll
+    for (int m = 0; m < 32; ++m) v[m] = lane + 32 * m < ne ? x[lane + 32 * m] : nan;
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+      mn = fminf(mn, v[m]);
+      mx = fmaxf(mx, v[m]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  float lo = -INFINITY, hi = INFINITY;
+  float span = mx - mn;
+  if (isfinite(mn) && isfinite(mx) && isfinite(span)) {
+    // the estimate's range widened by an eighth (half on each side), or
+    // narrow bins centred on a flat estimate
+    if (span > 0.f) {
+      mn -= span * 0.0625f;
+      span *= 1.125f;
+    } else {
+      span = fabsf(mn) * 0x1p-10f + 0x1p-100f;
+      mn -= 0.5f * span;
+    }
+    const float inv = float(kBrBins) / span;
+    for (int i = lane; i < kBrBins; i += 32) hist[i] = 0;
+    __syncwarp();
+    const int nf4 = S >> 2;
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    for (int f0 = 0; f0 < nf4; f0 += 32 * 8) {
+      float4 q4[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int f = f0 + 32 * u + lane;
+        q4[u] = f < nf4 ? x4[f] : make_float4(nan, nan, nan, nan);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float e[4] = {q4[u].x, q4[u].y, q4[u].z, q4[u].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (e[c] == e[c]) atomicAdd(&hist[lin_bin(e[c], mn, inv, kBrBins)], 1u);
+      }
+    }
+    for (int i = 4 * nf4 + lane; i < S; i += 32) {
+      const float v = x[i];
+      if (v == v) atomicAdd(&hist[lin_bin(v, mn, inv, kBrBins)], 1u);
+    }
+    __syncwarp();
+    constexpr int per = kBrBins / 32;
+    const int top = kBrBins - 1 - per * lane;  // lane 0 holds the highest bins
+    uint32_t tot = 0;
+#pragma unroll 8
+    for (int e = 0; e < per; ++e) tot += hist[top - e];
+    uint32_t c = warp_incl_scan(tot) - tot;  // samples in higher bins
+    float hv = INFINITY, lv = -INFINITY;
+    bool got_hi = false, got_lo = false;
+    for (int e = 0; e < per; ++e) {
+      const int bin = top - e;
+      const uint32_t n = hist[bin];
+      if (n > 0) {
+        if (r_hi >= float(c) && r_hi < float(c + n)) {
+          got_hi = true;
+          hv = bin == kBrBins - 1 ? INFINITY : mn + float(bin + 1) / inv;
+        }
+        if (r_lo >= float(c) && r_lo < float(c + n)) {
+          got_lo = true;
+          lv = bin == 0 ? -INFINITY : mn + float(bin) / inv;
+        }
+      }
+      c += n;
+    }
+    const unsigned bh_ = __ballot_sync(0xffffffffu, got_hi), bl_ = __ballot_sync(0xffffffffu, got_lo);
+    if (bh_) hi = __shfl_sync(0xffffffffu, hv, __ffs(bh_) - 1);
+    if (bl_) lo = __shfl_sync(0xffffffffu, lv, __ffs(bl_) - 1);
+    if (hi < lo) hi = lo;
+  }
+  if (lane == 0) lohi[row] = make_float2(lo, hi);
+}
+
+struct FinArgs {
+  int64_t rows, G, k;
+  int32_t Nk, nreg, cap, gchunks, all_keys;
+  const uint32_t* mask;
+  int64_t ld_mask;
+  const uint2* cand;
+  const int32_t* nabove;
+  const int32_t* ncand;
+  int32_t* col_idx;
+  int64_t col_capacity;
+  int64_t* counts;
+  int32_t* fail_rows;   // rows left to the score + select kernels
+  int32_t* fail_count;
+  int32_t* fail_units;  // [BH * gchunks] non-zero: that unit's scores are needed
+};
+constexpr int kFinCand = kWindow / 2;  // candidates held in the select's window storage
+constexpr int kFinEq = kBins;          // keys equal to the cut that can be ranked by index
+constexpr size_t kFinMaskOff = (sizeof(SelSmem) + 15) & ~size_t(15);  // the row's mask (uint4 copies)
+
+__global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const FinArgs a) {
+  extern __shared__ __align__(16) uint8_t fin_raw[];
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(fin_raw);
+  uint32_t* kept = reinterpret_cast<uint32_t*>(fin_raw + kFinMaskOff);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
+  const int64_t k = a.k, base = row * k;
+  if (a.all_keys) {  // k == Nk: every key, in order
+    if (base + k <= a.col_capacity)
+      for (int j = tid; j < a.Nk; j += kSelThreads) a.col_idx[base + j] = j;
+    if (tid == 0) a.counts[row] = k;
+    return;
+  }
+  const int32_t* nab = a.nabove + row * a.nreg;
+  const int32_t* ncd = a.ncand + row * a.nreg;
+  __shared__ int32_t reg_off[33];
+  if (tid < 32) {
+    int64_t above = 0;
+    int ntot = 0, over = 0;
+    for (int r = lane; r < a.nreg; r += 32) {  // (nreg <= 32)
+      above += nab[r];
+      const int c = ncd[r];
+      over |= c > a.cap;
+      ntot += c;
+    }
+    // region offsets in the packed candidate list
+    const int c = lane < a.nreg ? min(ncd[lane], a.cap) : 0;
+    const int incl = warp_incl_scan(c);
+    reg_off[lane + 1] = incl;
+    if (lane == 0) reg_off[0] = 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      above += __shfl_xor_sync(0xffffffffu, above, o);
+      ntot += __shfl_xor_sync(0xffffffffu, ntot, o);
+      over |= __shfl_xor_sync(0xffffffffu, over, o);
+    }
+    if (tid == 0) {
+      sm.found_above_cnt = above;
+      sm.n_win = ntot;
+      sm.found_cnt = over;
+    }
+  }
+  // the row goes to the score + select kernels
+  auto leave = [&]() {
+    if (tid == 0) {
+      const int32_t i = atomicAdd(a.fail_count, 1);
+      a.fail_rows[i] = static_cast<int32_t>(row);
+      const int64_t bh = row / a.G, g = row % a.G;
+      a.fail_units[bh * a.gchunks + g / 128] = 1;
+    }
+  };
+  __syncthreads();
+  const int64_t above = sm.found_above_cnt;
+  const int ntot = sm.n_win;
+  if (!(sm.found_cnt == 0 && above <= k && k <= above + ntot && ntot <= kFinCand)) {
+    leave();
+    return;
+  }
+  const int words = static_cast<int>((a.Nk + 31) / 32);
+  {  // the keys above the bracket
+    const uint4* mrow = reinterpret_cast<const uint4*>(a.mask + row * a.ld_mask);
+    for (int w = tid; w < static_cast<int>(a.ld_mask / 4); w += kSelThreads)
+      reinterpret_cast<uint4*>(kept)[w] = mrow[w];
+  }
+  int32_t* cj = sm.u.win.j;
+  float* cx = reinterpret_cast<float*>(sm.u.win.j + kFinCand);
+  const int64_t need = k - above;  // candidates to keep
+  if (need > 0) {
+    // candidate i of the packed list: region r with reg_off[r] <= i < reg_off[r+1];
+    // up to eight loads in flight per thread
+    const uint2* src = a.cand + row * int64_t(a.nreg) * a.cap;
+    for (int i0 = 0; i0 < ntot; i0 += 8 * kSelThreads) {
+      uint2 e[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kSelThreads + tid;
+        if (i < ntot) {
+          int r = 0;
+          while (reg_off[r + 1] <= i) ++r;
+          e[u] = src[int64_t(r) * a.cap + (i - reg_off[r])];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kSelThreads + tid;
+        if (i < ntot) {
+          cj[i] = static_cast<int32_t>(e[u].x);
+          cx[i] = __uint_as_float(e[u].y);
+        }
+      }
+    }
+    float wmn = INFINITY, wmx = -INFINITY;
+    for (int i = tid; i < ntot; i += kSelThreads) {
+      wmn = fminf(wmn, cx[i]);
+      wmx = fmaxf(wmx, cx[i]);
+    }
+    wmn = block_min(wmn, sm);  // (its barriers also publish cx, cj)
+    wmx = block_max(wmx, sm);
+    // The need-th candidate by (score descending, key ascending): one
+    // histogram over kBins linear bins of [wmn, wmx], the bin where the
+    // count from the top reaches need, then an exact ranking of that bin's
+    // candidates.  Equal scores share a bin; a bin too full to rank leaves
+    // the row to the select kernel.
+    uint32_t cut;
+    int64_t ties;
+    const bool flat = !(wmx > wmn);
+    const float inv = flat ? 0.f : float(kBins) / (wmx - wmn);
+    for (int i = tid; i < kBins; i += kSelThreads) sm.hist[i] = 0;
+    if (tid == 0) {
+      sm.claim = -1;
+      sm.n_rank = 0;
+      sm.cut_rank = -1;
+    }
+    __syncthreads();
+    if (!flat)
+      for (int i = tid; i < ntot; i += kSelThreads) atomicAdd(&sm.hist[lin_bin(cx[i], wmn, inv, kBins)], 1u);
+    else if (tid == 0)
+      sm.hist[0] = static_cast<uint32_t>(ntot);
+    __syncthreads();
+    const int top = kBins - 1 - kBinsPerThread * tid;  // thread 0 holds the highest bins
+    int64_t c4 = 0;
+#pragma unroll
+    for (int e = 0; e < kBinsPerThread; ++e) c4 += sm.hist[top - e];
+    int64_t ctot;
+    int64_t cum = block_excl_scan<int64_t>(c4, &ctot, sm.scan_c);
+    for (int e = 0; e < kBinsPerThread; ++e) {
+      const int bin = top - e;
+      const int64_t bc = sm.hist[bin];
+      if (bc > 0 && cum < need && cum + bc >= need) {
+        sm.claim = bin;
+        sm.found_above_cnt = cum;  // candidates in higher bins
+      }
+      cum += bc;
+    }
+    __syncthreads();
+    const int bin = sm.claim;
+    const int64_t higher = sm.found_above_cnt;
+    const int nb = bin >= 0 ? static_cast<int>(sm.hist[bin]) : 0;
+    if (bin < 0 || nb > kRank) {
+      leave();
+      return;
+    }
+    // the bin's candidates
+    for (int base_i = warp * 32; base_i < ntot; base_i += kSelThreads) {
+      const int i = base_i + lane;
+      const bool in = i < ntot && (flat || lin_bin(cx[i], wmn, inv, kBins) == bin);
+      const unsigned bal = __ballot_sync(0xffffffffu, in);
+      int s0 = 0;
+      if (lane == 0 && bal) s0 = atomicAdd(&sm.n_rank, __popc(bal));
+      const int slot = __shfl_sync(0xffffffffu, s0, 0) + __popc(bal & ((1u << lane) - 1u));
+      if (in && slot < kRank) {
+        sm.rx[slot] = cx[i];
+        sm.rj[slot] = cj[i];
+      }
+    }
+    __syncthreads();
+    for (int c = tid; c < nb; c += kSelThreads) {
+      const float xc = sm.rx[c];
+      const int jc = sm.rj[c];
+      int rank = 0, greater = 0;
+      for (int o = 0; o < nb; ++o) {
+        const float xo = sm.rx[o];
+        rank += xo > xc || (xo == xc && sm.rj[o] < jc);
+        greater += xo > xc;
+      }
+      if (higher + rank == need - 1) {
+        sm.cut_rank = rank;
+        sm.cut_x = xc;
+        sm.cut_greater = greater;
+      }
+    }
+    __syncthreads();
+    if (sm.cut_rank < 0) {  // (never)
+      leave();
+      return;
+    }
+    cut = order_key(sm.cut_x);
+    ties = need - (higher + sm.cut_greater);  // keys equal to the cut that are kept
+    // keys equal to the cut: all in this bin; the lowest indices are kept
+    int n_eq = 0;
+    for (int c = 0; c < nb; ++c) n_eq += order_key(sm.rx[c]) == cut;
+    const bool rank_ties = ties < n_eq;
+    for (int i = tid; i < ntot; i += kSelThreads) {
+      const uint32_t kx = order_key(cx[i]);
+      const int j = cj[i];
+      bool keep = kx > cut;
+      if (kx == cut) {
+        if (!rank_ties) {
+          keep = true;
+        } else {
+          int before = 0;  // lower indices first among equal scores
+          for (int c = 0; c < nb; ++c) before += order_key(sm.rx[c]) == cut && sm.rj[c] < j;
+          keep = before < ties;
+        }
+      }
+      if (keep) atomicOr(&kept[j >> 5], 1u << (j & 31));
+    }
+  }
+  __syncthreads();
+  // output offset of every mask word (the candidates' storage is free now);
+  // exactly k kept keys, or the row is left to the select kernel
+  int32_t* woff = sm.u.win.j;
+  const int per = (words + kSelThreads - 1) / kSelThreads;
+  const int wa = min(words, tid * per), wb = min(words, wa + per);
+  int64_t loc = 0;
+  for (int w = wa; w < wb; ++w) loc += __popc(kept[w]);
+  int64_t tot;
+  int64_t run = block_excl_scan<int64_t>(loc, &tot, sm.scan_c);
+  for (int w = wa; w < wb; ++w) {
+    woff[w] = static_cast<int32_t>(run);
+    run += __popc(kept[w]);
+  }
+  __syncthreads();
+  if (tot != k) {
+    leave();
+    return;
+  }
+  if (base + k <= a.col_capacity) {
+    // a word at a time per warp, lane = bit: each word's keys leave in one
+    // coalesced store whatever their density
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll 4
+    for (int w = warp; w < words; w += kSelWarps) {
+      const uint32_t e = kept[w];
+      if (e != 0u && ((e >> lane) & 1u)) a.col_idx[base + woff[w] + __popc(e & lt)] = w * 32 + lane;
+    }
+  }
+  if (tid == 0) a.counts[row] = k;
 }
 
 // ------------------------------------------------------------ validator
@@ -1175,23 +1867,36 @@ BuildLayout build_layout(int64_t rows, int32_t Nk, int32_t d) {
   off = align256(off + size_t(rows) * 8);
   L.misc = off;
   off = align256(off + 16);
+  L.fail = off;
+  off = align256(off + 256 + size_t(rows) * 8);
   L.total = off;
   return L;
 }
 
+// Scores of every stride-th key (nkeys of them per head; stride 1 and nkeys
+// Nk: every key) into `out`, fp32 [rows, ld]; only the units flagged in
+// unit_filter when it is given.
 template <int D>
-static cudaError_t launch_scores(const BuildArgs& a, int num_sms, cudaStream_t st, int32_t* status) {
+static cudaError_t launch_scores(const BuildArgs& a, int num_sms, cudaStream_t st, int32_t* status,
+                                 const int32_t* unit_filter = nullptr, float* out = nullptr,
+                                 int64_t ld = 0, int32_t nkeys = 0, int32_t stride = 1) {
   using C = ScoreCfg<D>;
+  if (!out) {
+    out = reinterpret_cast<float*>(a.ws + a.L.scores);
+    ld = a.L.ld;
+    nkeys = a.Nk;
+    stride = 1;
+  }
   ScoreArgs s;
   s.k = a.k;
   s.qhi = reinterpret_cast<const uint16_t*>(a.ws + a.L.qhi);
   s.qlo = reinterpret_cast<const uint16_t*>(a.ws + a.L.qlo);
-  s.scores = reinterpret_cast<float*>(a.ws + a.L.scores);
-  s.ld = a.L.ld;
+  s.scores = out;
+  s.ld = ld;
   s.G = a.G;
-  s.Nk = a.Nk;
+  s.Nk = nkeys;
   s.gchunks = static_cast<int32_t>((a.G + 127) / 128);
-  s.ntiles = (a.Nk + 127) / 128;
+  s.ntiles = (nkeys + 127) / 128;
   const int64_t base = int64_t(a.BH) * s.gchunks;
   int64_t ks = (2 * int64_t(num_sms) + base - 1) / base;
   ks = ks < 1 ? 1 : (ks > s.ntiles ? s.ntiles : ks);
@@ -1200,11 +1905,12 @@ static cudaError_t launch_scores(const BuildArgs& a, int num_sms, cudaStream_t s
   s.units = base * s.ksplit;
   s.scale = a.scale;
   s.status = status;
+  s.unit_filter = unit_filter;
   CUtensorMap tm_qhi, tm_qlo, tm_k, tm_out;
   if (!make_rows_map(&tm_qhi, s.qhi, uint64_t(a.rows), D, 128) ||
       !make_rows_map(&tm_qlo, s.qlo, uint64_t(a.rows), D, 128) ||
-      !make_rows_map(&tm_k, a.k, uint64_t(a.BH) * a.Nk, D, 128) ||
-      !make_scores_map(&tm_out, s.scores, static_cast<uint32_t>(a.Nk), uint64_t(a.G), uint64_t(a.BH),
+      !make_keys_map(&tm_k, a.k, D, uint64_t(nkeys), uint64_t(a.Nk), uint64_t(a.BH), uint64_t(stride)) ||
+      !make_scores_map(&tm_out, s.scores, static_cast<uint32_t>(nkeys), uint64_t(a.G), uint64_t(a.BH),
                        uint64_t(s.ld)))
     return cudaErrorInvalidValue;
   auto kern = sa_score_kernel<D>;
@@ -1218,16 +1924,183 @@ static cudaError_t launch_scores(const BuildArgs& a, int num_sms, cudaStream_t s
 cudaError_t launch_colstat(const BuildArgs& b, float* scores, int32_t* status, int num_sms,
                            cudaStream_t st);
 
+// Key splits of a score pass over ntiles tiles of 128 keys: about two units
+// per SM, as for the score kernel.
+static void split_keys(int64_t base, int ntiles, int num_sms, int32_t* tps, int32_t* ksplit) {
+  int64_t ks = (2 * int64_t(num_sms) + base - 1) / base;
+  ks = ks < 1 ? 1 : (ks > ntiles ? ntiles : ks);
+  *tps = static_cast<int32_t>((ntiles + ks - 1) / ks);
+  *ksplit = (ntiles + *tps - 1) / *tps;
+}
+
+// Buffers of the TOPK path without a score matrix, carved from the scores
+// region of the workspace; ok = false when they do not fit (the score matrix
+// path is used instead).
+struct TopkPlan {
+  bool ok = false;
+  int32_t stride = 8, S = 0, gchunks = 0;
+  int32_t ksplit = 0, ntiles = 0;  // classifying pass
+  int32_t nreg = 0, cap = 0;       // candidate regions per row, slots per region
+  int64_t ld_samp = 0, ld_mask = 0;
+  float r_hi = 0.f, r_lo = 0.f;
+  size_t samp = 0, lohi = 0, mask = 0, cand = 0, nabove = 0, ncand = 0;
+};
+
+static TopkPlan plan_topk(const BuildArgs& a, int num_sms) {
+  TopkPlan P;
+  const int64_t k = a.topk;
+  // (a whole number of samples per head keeps the strided key map's head
+  // stride a multiple of its row stride)
+  if (a.Nk < 8192 || a.Nk % P.stride != 0 || k >= a.Nk || k < 1 || !(a.scale > 0.f)) return P;
+  P.gchunks = static_cast<int32_t>((a.G + 127) / 128);
+  const int64_t base = int64_t(a.BH) * P.gchunks;
+  P.S = a.Nk / P.stride;
+  P.ntiles = (a.Nk + 127) / 128;
+  int32_t tps;
+  split_keys(base, P.ntiles, num_sms, &tps, &P.ksplit);
+  P.ksplit = P.ksplit > 8 ? 8 : P.ksplit;  // at most 16 candidate regions per row
+  P.nreg = 2 * P.ksplit;
+  P.ld_samp = (int64_t(P.S) + 3) & ~int64_t(3);
+  P.ld_mask = int64_t(P.ntiles) * 4;
+  // The cut's sample rank (from the top) is binomial around p: bracket it by
+  // four standard deviations and 16 ranks each way.
+  const double q = double(k) / double(a.Nk), p = q * P.S;
+  const double dev = 4.0 * sqrt(double(P.S) * q * (1.0 - q)) + 16.0;
+  P.r_hi = static_cast<float>(p - dev);
+  P.r_lo = static_cast<float>(p + dev);
+  // expected keys in the bracket; the finalize takes up to kFinCand of them
+  const double window = (2.0 * dev / P.S) * a.Nk;
+  if (window > 0.85 * kFinCand) return P;  // the bracket would often overflow the finalize
+  // the row's mask in shared memory, its word offsets in the window storage
+  if (kFinMaskOff + size_t(P.ld_mask) * 4 > 160 * 1024 || P.ld_mask > kWindow) return P;
+  const size_t rows = size_t(a.rows);
+  size_t off = 0;
+  P.samp = off;
+  off = align256(off + rows * size_t(P.ld_samp) * 4);
+  P.lohi = off;
+  off = align256(off + rows * 8);
+  P.mask = off;
+  off = align256(off + rows * size_t(P.ld_mask) * 4);
+  P.nabove = off;
+  off = align256(off + rows * size_t(P.nreg) * 4);
+  P.ncand = off;
+  off = align256(off + rows * size_t(P.nreg) * 4);
+  P.cand = off;
+  // the regions take what the scores region still holds, up to kFinCand each;
+  // their expected share of the bracket (tiles spread over the sequence) must
+  // fit twice over, plus 96
+  const size_t region = rows * size_t(a.L.ld) * 4;
+  if (off >= region) return P;
+  const int64_t room = static_cast<int64_t>((region - off) / (rows * size_t(P.nreg) * 8));
+  P.cap = static_cast<int32_t>(room < kFinCand ? room : kFinCand);
+  P.ok = P.cap >= 2.0 * window / P.nreg + 96;
+  return P;
+}
+
+template <int D>
+static cudaError_t launch_rowscore(const BuildArgs& a, const TopkPlan& P, int num_sms, cudaStream_t st,
+                                   int32_t* status) {
+  using C = RowScoreCfg<D>;
+  uint8_t* reg = a.ws + a.L.scores;
+  RowScoreArgs r;
+  r.G = a.G;
+  r.Nk = a.Nk;
+  r.gchunks = P.gchunks;
+  r.ntiles = P.ntiles;
+  r.ksplit = P.ksplit;
+  r.units = int64_t(a.BH) * P.gchunks * r.ksplit;
+  r.scale = a.scale;
+  r.lohi = reinterpret_cast<const float2*>(reg + P.lohi);
+  r.mask = reinterpret_cast<uint32_t*>(reg + P.mask);
+  r.ld_mask = P.ld_mask;
+  r.cand = reinterpret_cast<uint2*>(reg + P.cand);
+  r.cap = P.cap;
+  r.nabove = reinterpret_cast<int32_t*>(reg + P.nabove);
+  r.ncand = reinterpret_cast<int32_t*>(reg + P.ncand);
+  r.status = status;
+  CUtensorMap tm_qhi, tm_qlo, tm_k;
+  if (!make_rows_map(&tm_qhi, a.ws + a.L.qhi, uint64_t(a.rows), D, 128) ||
+      !make_rows_map(&tm_qlo, a.ws + a.L.qlo, uint64_t(a.rows), D, 128) ||
+      !make_keys_map(&tm_k, a.k, D, uint64_t(a.Nk), uint64_t(a.Nk), uint64_t(a.BH), 1u))
+    return cudaErrorInvalidValue;
+  auto kern = sa_rowscore_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = r.units < num_sms ? r.units : num_sms;
+  kern<<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, st>>>(r, tm_qhi, tm_qlo, tm_k);
+  return cudaGetLastError();
+}
+
+// TOPK lists without the score matrix (see section 6); rows it cannot
+// bracket go through the score and select kernels afterwards.
+static cudaError_t launch_topk_direct(const BuildArgs& a, const TopkPlan& P, bool all_keys,
+                                      int num_sms, cudaStream_t st, int32_t* status) {
+  cudaError_t e;
+  uint8_t* reg = a.ws + a.L.scores;
+  int32_t* fail_count = reinterpret_cast<int32_t*>(a.ws + a.L.fail);
+  int32_t* fail_rows = reinterpret_cast<int32_t*>(a.ws + a.L.fail + 256);
+  int32_t* fail_units = fail_rows + a.rows;
+  if (!all_keys) {
+    float* samp = reinterpret_cast<float*>(reg + P.samp);
+    e = a.d == 128 ? launch_scores<128>(a, num_sms, st, status, nullptr, samp, P.ld_samp, P.S, P.stride)
+                   : launch_scores<64>(a, num_sms, st, status, nullptr, samp, P.ld_samp, P.S, P.stride);
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = (a.rows + kBrWarps - 1) / kBrWarps;
+    sa_bracket_kernel<<<static_cast<unsigned>(blocks), 32 * kBrWarps, 0, st>>>(
+        reinterpret_cast<const float*>(reg + P.samp), P.ld_samp, P.S, a.rows, P.r_hi, P.r_lo,
+        reinterpret_cast<float2*>(reg + P.lohi));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = a.d == 128 ? launch_rowscore<128>(a, P, num_sms, st, status)
+                   : launch_rowscore<64>(a, P, num_sms, st, status);
+    if (e != cudaSuccess) return e;
+    // fail count and unit flags start at zero (the rows list needs no clearing)
+    if ((e = cudaMemsetAsync(fail_count, 0, 4, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(fail_units, 0, size_t(a.rows) * 4, st)) != cudaSuccess) return e;
+  }
+  FinArgs f;
+  f.rows = a.rows;
+  f.G = a.G;
+  f.k = all_keys ? a.Nk : a.topk;
+  f.Nk = a.Nk;
+  f.nreg = P.nreg;
+  f.cap = P.cap;
+  f.gchunks = P.gchunks;
+  f.all_keys = all_keys ? 1 : 0;
+  f.mask = reinterpret_cast<const uint32_t*>(reg + P.mask);
+  f.ld_mask = P.ld_mask;
+  f.cand = reinterpret_cast<const uint2*>(reg + P.cand);
+  f.nabove = reinterpret_cast<const int32_t*>(reg + P.nabove);
+  f.ncand = reinterpret_cast<const int32_t*>(reg + P.ncand);
+  f.col_idx = a.col_idx;
+  f.col_capacity = a.col_capacity;
+  f.counts = reinterpret_cast<int64_t*>(a.ws + a.L.counts);
+  f.fail_rows = fail_rows;
+  f.fail_count = fail_count;
+  f.fail_units = fail_units;
+  const size_t fin_smem = all_keys ? 0 : kFinMaskOff + size_t(P.ld_mask) * 4;
+  e = cudaFuncSetAttribute(sa_topk_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(fin_smem));
+  if (e != cudaSuccess) return e;
+  sa_topk_finalize_kernel<<<static_cast<unsigned>(a.rows), kSelThreads, fin_smem, st>>>(f);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_build_index(const BuildArgs& a, int num_sms, cudaStream_t st) {
   int64_t* misc = reinterpret_cast<int64_t*>(a.ws + a.L.misc);
   int32_t* status = reinterpret_cast<int32_t*>(misc + 1);
   cudaError_t e = cudaMemsetAsync(misc, 0, 16, st);
   if (e != cudaSuccess) return e;
+  // TOPK by mean query: lists without the score matrix when its buffers fit
+  const bool topk = a.stat < 0 && a.mode == SA_SELECT_TOPK;
+  const bool all_keys = topk && a.topk >= a.Nk;
+  TopkPlan P;
+  if (topk && !all_keys) P = plan_topk(a, num_sms);
+  const bool direct = all_keys || P.ok;
   if (a.stat >= 0) {
     // dense-step statistics of the full attention probabilities
     e = launch_colstat(a, reinterpret_cast<float*>(a.ws + a.L.scores), status, num_sms, st);
     if (e != cudaSuccess) return e;
-  } else {
+  } else if (!all_keys) {
     uint16_t* qhi = reinterpret_cast<uint16_t*>(a.ws + a.L.qhi);
     uint16_t* qlo = reinterpret_cast<uint16_t*>(a.ws + a.L.qlo);
     if (a.d == 128)
@@ -1235,7 +2108,19 @@ cudaError_t launch_build_index(const BuildArgs& a, int num_sms, cudaStream_t st)
     else
       sa_meanq_kernel<64><<<static_cast<unsigned>(a.rows), 256, 0, st>>>(a.q, qhi, qlo, a.G, a.Nq, a.M);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    e = a.d == 128 ? launch_scores<128>(a, num_sms, st, status) : launch_scores<64>(a, num_sms, st, status);
+    if (direct) {
+      e = launch_topk_direct(a, P, false, num_sms, st, status);
+      if (e != cudaSuccess) return e;
+      // the rows it left: their units' scores, then the select kernel on them
+      const int32_t* fail_units = reinterpret_cast<const int32_t*>(a.ws + a.L.fail + 256) + a.rows;
+      e = a.d == 128 ? launch_scores<128>(a, num_sms, st, status, fail_units)
+                     : launch_scores<64>(a, num_sms, st, status, fail_units);
+    } else {
+      e = a.d == 128 ? launch_scores<128>(a, num_sms, st, status) : launch_scores<64>(a, num_sms, st, status);
+    }
+    if (e != cudaSuccess) return e;
+  } else {
+    e = launch_topk_direct(a, P, true, num_sms, st, status);
     if (e != cudaSuccess) return e;
   }
   SelArgs s;
@@ -1257,11 +2142,19 @@ cudaError_t launch_build_index(const BuildArgs& a, int num_sms, cudaStream_t st)
   const int words = (a.Nk + 31) / 32;
   s.mask_words = (a.mode == SA_SELECT_TOPK && sizeof(SelSmem) + size_t(words) * 4 <= kSelSmemBudget) ? words : 0;
   const size_t sel_smem = sizeof(SelSmem) + size_t(s.mask_words) * 4;
-  e = cudaFuncSetAttribute(sa_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sel_smem));
-  if (e != cudaSuccess) return e;
-  sa_select_kernel<<<static_cast<unsigned>(a.rows), kSelThreads, sel_smem, st>>>(s);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (!all_keys) {
+    auto kern = direct ? sa_select_kernel<true> : sa_select_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sel_smem));
+    if (e != cudaSuccess) return e;
+    int64_t grid = a.rows;
+    if (direct) {  // only the rows the direct path left
+      s.row_count = reinterpret_cast<const int32_t*>(a.ws + a.L.fail);
+      s.row_list = s.row_count + 64;
+      grid = a.rows < 4 * int64_t(num_sms) ? a.rows : 4 * int64_t(num_sms);
+    }
+    kern<<<static_cast<unsigned>(grid), kSelThreads, sel_smem, st>>>(s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   sa_scan_kernel<<<1, 1024, 0, st>>>(s.counts, a.rows, a.row_ptr, misc, a.col_capacity, status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (a.mode != SA_SELECT_TOPK)

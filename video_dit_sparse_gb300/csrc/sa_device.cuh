@@ -153,6 +153,16 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int x
       : "memory");
 }
 
+// 3-D tiled TMA load of one box at element coordinates (x, y, z).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 3-D tiled TMA store of one box from shared memory (bulk async group).
 __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int x, int y, int z) {
   asm volatile(
@@ -391,6 +401,25 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
 __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// The bits of each half of a pair.
+__device__ __forceinline__ uint32_t f2lo_bits(uint64_t v) { return static_cast<uint32_t>(v); }
+__device__ __forceinline__ uint32_t f2hi_bits(uint64_t v) { return static_cast<uint32_t>(v >> 32); }
+// (w << 1) | (sign bit of x): one funnel shift
+__device__ __forceinline__ uint32_t shl_in(uint32_t w, uint32_t x) {
+  uint32_t r;
+  asm("shf.l.clamp.b32 %0, %1, %2, 1;" : "=r"(r) : "r"(x), "r"(w));
   return r;
 }
 __device__ __forceinline__ float fmax3(float a, float b, float c) {

@@ -40,8 +40,13 @@ cudaError_t launch_forward_delta(const FwdArgs& a, int d, int num_sms, cudaStrea
 //   ties       int32 [rows]     keys equal to the cut that are kept
 //   counts     int64 [rows]     kept keys per row
 //   misc       int64 nnz, int32 status
+//   fail       int32 count (own 256 bytes), int32 [rows] rows, int32 [rows] units:
+//              rows the TOPK path without a score matrix leaves to the select
+//              kernel, and the (head, 128-row chunk) units whose scores they need
+// The TOPK path without a score matrix keeps its sample scores, brackets,
+// keep-masks and candidates inside the scores region.
 struct BuildLayout {
-  size_t qhi, qlo, scores, cut, ties, counts, misc, total;
+  size_t qhi, qlo, scores, cut, ties, counts, misc, fail, total;
   int64_t ld;
 };
 BuildLayout build_layout(int64_t rows, int32_t Nk, int32_t d);

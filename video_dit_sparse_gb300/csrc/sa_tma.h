@@ -44,6 +44,22 @@ inline bool make_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Every `stride`-th key row of each of BH heads of a [BH, Nk, d] bf16 tensor:
+// row i of head h is key i*stride (i < nkeys), seen as boxes of 64 elements x
+// 128 rows of one head, 128-byte swizzled.  Rows past nkeys read as zeros.
+inline bool make_keys_map(CUtensorMap* map, const void* base, uint32_t d, uint64_t nkeys,
+                          uint64_t Nk, uint64_t BH, uint64_t stride) {
+  const EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d, nkeys, BH};
+  const cuuint64_t strides[2] = {stride * d * 2, Nk * d * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The fp32 score matrix of B*H heads x G rows x Nk keys (row stride ld
 // floats, head stride G*ld floats) seen as boxes of 32 keys x 128 rows of one
 // head, unswizzled.  Stores clip at Nk, at G (never into the next head) and
