@@ -103,8 +103,12 @@ typedef struct {
 
 /*
  * Bytes of device workspace sparse_attn_build_index needs for this problem
- * (mean queries, the fp32 score matrix of every group against every key,
- * per-row selection results and counters).  0 if the problem is invalid.
+ * (mean queries, room for the fp32 score matrix of every group against every
+ * key, per-row selection results, counters and a list of rows).  TOPK over
+ * at least 8192 keys uses the score matrix's room for smaller buffers (a
+ * sampled score matrix, per-row brackets, keep-masks and candidates) and
+ * writes full score rows only for rows those cannot settle.  0 if the
+ * problem is invalid.
  */
 size_t sparse_attn_build_index_workspace_size(const sa_problem* problem);
 
@@ -122,6 +126,12 @@ size_t sparse_attn_build_index_workspace_size(const sa_problem* problem);
  * (row_ptr[0] = 0, row_ptr[rows] = nnz).  Scores are computed in fp32 from
  * an fp32 mean query (split into two bf16 terms for the tensor cores), so a
  * key whose score lies within rounding of the cut may fall either side.
+ * TOPK over at least 8192 keys (a multiple of 8, scale > 0) finds each row's
+ * cut without storing the scores: a sample of every 8th key brackets the
+ * cut, a second scoring pass marks the keys above the bracket and keeps
+ * those inside it, and the exact cut is taken among them; rows whose bracket
+ * misses are selected from their full scores afterwards, so the lists are
+ * the same as by full sorting in every case.
  *
  *  q, k          device bf16 [B,H,Nq,d], [B,H,Nk,d]
  *  row_ptr       device int64 [B*H*G + 1], written

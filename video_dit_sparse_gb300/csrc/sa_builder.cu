@@ -1588,7 +1588,6 @@ struct FinArgs {
   int32_t* fail_units;  // [BH * gchunks] non-zero: that unit's scores are needed
 };
 constexpr int kFinCand = kWindow / 2;  // candidates held in the select's window storage
-constexpr int kFinEq = kBins;          // keys equal to the cut that can be ranked by index
 constexpr size_t kFinMaskOff = (sizeof(SelSmem) + 15) & ~size_t(15);  // the row's mask (uint4 copies)
 
 __global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const FinArgs a) {
@@ -1606,20 +1605,23 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const 
   }
   const int32_t* nab = a.nabove + row * a.nreg;
   const int32_t* ncd = a.ncand + row * a.nreg;
-  __shared__ int32_t reg_off[33];
+  __shared__ int32_t reg_off[65];
   if (tid < 32) {
     int64_t above = 0;
     int ntot = 0, over = 0;
-    for (int r = lane; r < a.nreg; r += 32) {  // (nreg <= 32)
+    for (int r = lane; r < a.nreg; r += 32) {  // (nreg <= 64)
       above += nab[r];
       const int c = ncd[r];
       over |= c > a.cap;
       ntot += c;
     }
     // region offsets in the packed candidate list
-    const int c = lane < a.nreg ? min(ncd[lane], a.cap) : 0;
-    const int incl = warp_incl_scan(c);
-    reg_off[lane + 1] = incl;
+    const int ca = lane < a.nreg ? min(ncd[lane], a.cap) : 0;
+    const int cb = lane + 32 < a.nreg ? min(ncd[lane + 32], a.cap) : 0;
+    const int ia = warp_incl_scan(ca);
+    const int ib = warp_incl_scan(cb) + __shfl_sync(0xffffffffu, ia, 31);
+    reg_off[lane + 1] = ia;
+    reg_off[lane + 33] = ib;
     if (lane == 0) reg_off[0] = 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -1668,8 +1670,10 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const 
       for (int u = 0; u < 8; ++u) {
         const int i = i0 + u * kSelThreads + tid;
         if (i < ntot) {
-          int r = 0;
-          while (reg_off[r + 1] <= i) ++r;
+          int r = 0;  // the last region with reg_off[r] <= i
+#pragma unroll
+          for (int step = 32; step > 0; step >>= 1)
+            if (r + step < a.nreg && reg_off[r + step] <= i) r += step;
           e[u] = src[int64_t(r) * a.cap + (i - reg_off[r])];
         }
       }
@@ -1924,15 +1928,6 @@ static cudaError_t launch_scores(const BuildArgs& a, int num_sms, cudaStream_t s
 cudaError_t launch_colstat(const BuildArgs& b, float* scores, int32_t* status, int num_sms,
                            cudaStream_t st);
 
-// Key splits of a score pass over ntiles tiles of 128 keys: about two units
-// per SM, as for the score kernel.
-static void split_keys(int64_t base, int ntiles, int num_sms, int32_t* tps, int32_t* ksplit) {
-  int64_t ks = (2 * int64_t(num_sms) + base - 1) / base;
-  ks = ks < 1 ? 1 : (ks > ntiles ? ntiles : ks);
-  *tps = static_cast<int32_t>((ntiles + ks - 1) / ks);
-  *ksplit = (ntiles + *tps - 1) / *tps;
-}
-
 // Buffers of the TOPK path without a score matrix, carved from the scores
 // region of the workspace; ok = false when they do not fit (the score matrix
 // path is used instead).
@@ -1956,10 +1951,6 @@ static TopkPlan plan_topk(const BuildArgs& a, int num_sms) {
   const int64_t base = int64_t(a.BH) * P.gchunks;
   P.S = a.Nk / P.stride;
   P.ntiles = (a.Nk + 127) / 128;
-  int32_t tps;
-  split_keys(base, P.ntiles, num_sms, &tps, &P.ksplit);
-  P.ksplit = P.ksplit > 8 ? 8 : P.ksplit;  // at most 16 candidate regions per row
-  P.nreg = 2 * P.ksplit;
   P.ld_samp = (int64_t(P.S) + 3) & ~int64_t(3);
   P.ld_mask = int64_t(P.ntiles) * 4;
   // The cut's sample rank (from the top) is binomial around p: bracket it by
@@ -1973,27 +1964,46 @@ static TopkPlan plan_topk(const BuildArgs& a, int num_sms) {
   if (window > 0.85 * kFinCand) return P;  // the bracket would often overflow the finalize
   // the row's mask in shared memory, its word offsets in the window storage
   if (kFinMaskOff + size_t(P.ld_mask) * 4 > 160 * 1024 || P.ld_mask > kWindow) return P;
-  const size_t rows = size_t(a.rows);
-  size_t off = 0;
-  P.samp = off;
-  off = align256(off + rows * size_t(P.ld_samp) * 4);
-  P.lohi = off;
-  off = align256(off + rows * 8);
-  P.mask = off;
-  off = align256(off + rows * size_t(P.ld_mask) * 4);
-  P.nabove = off;
-  off = align256(off + rows * size_t(P.nreg) * 4);
-  P.ncand = off;
-  off = align256(off + rows * size_t(P.nreg) * 4);
-  P.cand = off;
-  // the regions take what the scores region still holds, up to kFinCand each;
-  // their expected share of the bracket (tiles spread over the sequence) must
-  // fit twice over, plus 96
-  const size_t region = rows * size_t(a.L.ld) * 4;
-  if (off >= region) return P;
-  const int64_t room = static_cast<int64_t>((region - off) / (rows * size_t(P.nreg) * 8));
-  P.cap = static_cast<int32_t>(room < kFinCand ? room : kFinCand);
-  P.ok = P.cap >= 2.0 * window / P.nreg + 96;
+  const size_t rows = size_t(a.rows), region = rows * size_t(a.L.ld) * 4;
+  // Key splits: among the counts (at most 32, so at most 64 candidate regions
+  // per row) whose regions fit the scores region, the one that minimises the
+  // tiles of the busiest SM, counting two tiles of start-up per unit.  A
+  // region takes what the scores region holds, up to kFinCand slots; its
+  // expected share of the bracket (tiles spread over the sequence) must fit
+  // twice over, plus 96.
+  int64_t best = -1;
+  for (int ks = 1; ks <= 32 && ks <= P.ntiles; ++ks) {
+    const int nreg = 2 * ks;
+    size_t off = 0;
+    const size_t samp = off;
+    off = align256(off + rows * size_t(P.ld_samp) * 4);
+    const size_t lohi = off;
+    off = align256(off + rows * 8);
+    const size_t mask = off;
+    off = align256(off + rows * size_t(P.ld_mask) * 4);
+    const size_t nab = off;
+    off = align256(off + rows * size_t(nreg) * 4);
+    const size_t ncd = off;
+    off = align256(off + rows * size_t(nreg) * 4);
+    if (off >= region) break;  // (more regions only take more room)
+    const int64_t room = static_cast<int64_t>((region - off) / (rows * size_t(nreg) * 8));
+    const int64_t cap = room < kFinCand ? room : kFinCand;
+    if (cap < 2.0 * window / nreg + 96) continue;
+    const int64_t units = base * ks, waves = (units + num_sms - 1) / num_sms;
+    const int64_t cost = waves * ((P.ntiles + ks - 1) / ks + 2);
+    if (best >= 0 && cost >= best) continue;
+    best = cost;
+    P.ksplit = ks;
+    P.nreg = nreg;
+    P.cap = static_cast<int32_t>(cap);
+    P.samp = samp;
+    P.lohi = lohi;
+    P.mask = mask;
+    P.nabove = nab;
+    P.ncand = ncd;
+    P.cand = off;
+    P.ok = true;
+  }
   return P;
 }
 
