@@ -406,7 +406,8 @@ struct RowIdxSrc {
   __device__ __forceinline__ int j(int i) const { return js[i]; }
 };
 
-__device__ __forceinline__ float block_min(float v, SelSmem& sm) {
+template <class Sm>
+__device__ __forceinline__ float block_min(float v, Sm& sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -418,7 +419,8 @@ __device__ __forceinline__ float block_min(float v, SelSmem& sm) {
   for (int w = 1; w < kSelWarps; ++w) v = fminf(v, sm.fred[0][w]);
   return v;
 }
-__device__ __forceinline__ float block_max(float v, SelSmem& sm) { return -block_min(-v, sm); }
+template <class Sm>
+__device__ __forceinline__ float block_max(float v, Sm& sm) { return -block_min(-v, sm); }
 
 __device__ __forceinline__ float f4_get(const float4& v, int e) {
   return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
@@ -1583,20 +1585,42 @@ struct FinArgs {
   int32_t* col_idx;
   int64_t col_capacity;
   int64_t* counts;
+  int64_t* row_ptr;     // TOPK: every row holds k keys, so row_ptr[r] = r * k
+  int64_t* nnz;
   int32_t* fail_rows;   // rows left to the score + select kernels
   int32_t* fail_count;
   int32_t* fail_units;  // [BH * gchunks] non-zero: that unit's scores are needed
 };
-constexpr int kFinCand = kWindow / 2;  // candidates held in the select's window storage
-constexpr size_t kFinMaskOff = (sizeof(SelSmem) + 15) & ~size_t(15);  // the row's mask (uint4 copies)
+constexpr int kFinCand = kWindow / 2;  // candidates a row may hold
+// The finalize's shared memory (then the row's keep-mask, 16-byte aligned):
+// small enough for four blocks per SM
+struct FinSmem {
+  uint32_t hist[kBins];
+  float rx[kRank];
+  int32_t rj[kRank];
+  int32_t cand[2 * kFinCand];  // keys, then scores; afterwards the mask words' offsets
+  float fred[3][32];
+  int64_t scan_c[32];
+  int64_t found_above_cnt, cut_greater;
+  int32_t claim, n_rank, cut_rank, n_win, found_cnt;
+  float cut_x;
+};
+constexpr size_t kFinMaskOff = (sizeof(FinSmem) + 15) & ~size_t(15);
 
 __global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const FinArgs a) {
   extern __shared__ __align__(16) uint8_t fin_raw[];
-  SelSmem& sm = *reinterpret_cast<SelSmem*>(fin_raw);
+  FinSmem& sm = *reinterpret_cast<FinSmem*>(fin_raw);
   uint32_t* kept = reinterpret_cast<uint32_t*>(fin_raw + kFinMaskOff);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.x;
   const int64_t k = a.k, base = row * k;
+  if (tid == 0) {
+    a.row_ptr[row] = base;
+    if (row == 0) {
+      a.row_ptr[a.rows] = a.rows * k;
+      *a.nnz = a.rows * k;
+    }
+  }
   if (a.all_keys) {  // k == Nk: every key, in order
     if (base + k <= a.col_capacity)
       for (int j = tid; j < a.Nk; j += kSelThreads) a.col_idx[base + j] = j;
@@ -1657,8 +1681,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const 
     for (int w = tid; w < static_cast<int>(a.ld_mask / 4); w += kSelThreads)
       reinterpret_cast<uint4*>(kept)[w] = mrow[w];
   }
-  int32_t* cj = sm.u.win.j;
-  float* cx = reinterpret_cast<float*>(sm.u.win.j + kFinCand);
+  int32_t* cj = sm.cand;
+  float* cx = reinterpret_cast<float*>(sm.cand + kFinCand);
   const int64_t need = k - above;  // candidates to keep
   if (need > 0) {
     // candidate i of the packed list: region r with reg_off[r] <= i < reg_off[r+1];
@@ -1796,7 +1820,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const 
   __syncthreads();
   // output offset of every mask word (the candidates' storage is free now);
   // exactly k kept keys, or the row is left to the select kernel
-  int32_t* woff = sm.u.win.j;
+  int32_t* woff = sm.cand;
   const int per = (words + kSelThreads - 1) / kSelThreads;
   const int wa = min(words, tid * per), wb = min(words, wa + per);
   int64_t loc = 0;
@@ -1963,7 +1987,7 @@ static TopkPlan plan_topk(const BuildArgs& a, int num_sms) {
   const double window = (2.0 * dev / P.S) * a.Nk;
   if (window > 0.85 * kFinCand) return P;  // the bracket would often overflow the finalize
   // the row's mask in shared memory, its word offsets in the window storage
-  if (kFinMaskOff + size_t(P.ld_mask) * 4 > 160 * 1024 || P.ld_mask > kWindow) return P;
+  if (kFinMaskOff + size_t(P.ld_mask) * 4 > 160 * 1024 || P.ld_mask > 2 * kFinCand) return P;
   const size_t rows = size_t(a.rows), region = rows * size_t(a.L.ld) * 4;
   // Key splits: among the counts (at most 32, so at most 64 candidate regions
   // per row) whose regions fit the scores region, the one that minimises the
@@ -2084,6 +2108,8 @@ static cudaError_t launch_topk_direct(const BuildArgs& a, const TopkPlan& P, boo
   f.col_idx = a.col_idx;
   f.col_capacity = a.col_capacity;
   f.counts = reinterpret_cast<int64_t*>(a.ws + a.L.counts);
+  f.row_ptr = a.row_ptr;
+  f.nnz = reinterpret_cast<int64_t*>(a.ws + a.L.misc);
   f.fail_rows = fail_rows;
   f.fail_count = fail_count;
   f.fail_units = fail_units;
@@ -2165,8 +2191,10 @@ cudaError_t launch_build_index(const BuildArgs& a, int num_sms, cudaStream_t st)
     kern<<<static_cast<unsigned>(grid), kSelThreads, sel_smem, st>>>(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  sa_scan_kernel<<<1, 1024, 0, st>>>(s.counts, a.rows, a.row_ptr, misc, a.col_capacity, status);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (!direct) {  // (the TOPK path's finalize writes row_ptr and nnz)
+    sa_scan_kernel<<<1, 1024, 0, st>>>(s.counts, a.rows, a.row_ptr, misc, a.col_capacity, status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if (a.mode != SA_SELECT_TOPK)
     sa_emit_kernel<<<static_cast<unsigned>(a.rows), kSelThreads, 0, st>>>(
         s.scores, s.ld, a.Nk, s.cut, s.ties, a.row_ptr, a.col_idx, a.col_capacity);
