@@ -41,7 +41,7 @@ def kernels_per_step(mode: str, topk: int = 0, Nk: int = 0) -> int:
     """Our kernels per step.  TOPK by mean query over at least 8192 keys (a
     multiple of 8): mean query, sample scores, bracket, classifying scores,
     finalize, the score and select kernels on the rows it left (usually
-    none), scan, forward; keeping every key: finalize, scan, forward.  Other
+    none), forward; keeping every key: finalize, forward.  Other
     selections: mean query, scores, select, scan, [emit,] forward (TOPK lists
     are written by the select kernel; the other modes add the emit kernel
     once the row offsets are known).  Dense-step workloads: dense forward,
@@ -53,8 +53,8 @@ def kernels_per_step(mode: str, topk: int = 0, Nk: int = 0) -> int:
         return 6
     if mode == "topk":
         if topk >= Nk:
-            return 3
-        return 9 if Nk >= 8192 and Nk % 8 == 0 else 5
+            return 2
+        return 8 if Nk >= 8192 and Nk % 8 == 0 else 5
     return 6
 
 
