@@ -1365,12 +1365,22 @@ __global__ void __launch_bounds__(RowScoreCfg<D>::kThreads, 1)
           const float* st = reinterpret_cast<const float*>(st4);
           uint64_t cm = (static_cast<uint64_t>(cw[1]) << 32) | cw[0];
           while (cm) {
+            // two candidates leave in one 16-byte store when the slot is even
+            // (region bases are 16-byte aligned: cap is even)
             const int c = __ffsll(static_cast<long long>(cm)) - 1;
             cm &= cm - 1;
-            if (nc < cap)
-              cbase[nc] = make_uint2(static_cast<uint32_t>(j0 + c),
-                                     __float_as_uint(st[((c >> 2) * 32 + lane) * 4 + (c & 3)] * a.scale));
-            ++nc;
+            const uint2 e1 = make_uint2(static_cast<uint32_t>(j0 + c),
+                                        __float_as_uint(st[((c >> 2) * 32 + lane) * 4 + (c & 3)] * a.scale));
+            if ((nc & 1) == 0 && cm != 0ull && nc + 1 < cap) {
+              const int c2 = __ffsll(static_cast<long long>(cm)) - 1;
+              cm &= cm - 1;
+              const uint32_t v2 = __float_as_uint(st[((c2 >> 2) * 32 + lane) * 4 + (c2 & 3)] * a.scale);
+              *reinterpret_cast<uint4*>(cbase + nc) = make_uint4(e1.x, e1.y, static_cast<uint32_t>(j0 + c2), v2);
+              nc += 2;
+            } else {
+              if (nc < cap) cbase[nc] = e1;
+              ++nc;
+            }
           }
           __syncwarp();
         }
@@ -1818,34 +1828,17 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const 
     }
   }
   __syncthreads();
-  // output offset of every mask word (the candidates' storage is free now);
   // exactly k kept keys, or the row is left to the select kernel
-  int32_t* woff = sm.cand;
-  const int per = (words + kSelThreads - 1) / kSelThreads;
-  const int wa = min(words, tid * per), wb = min(words, wa + per);
-  int64_t loc = 0;
-  for (int w = wa; w < wb; ++w) loc += __popc(kept[w]);
+  int pc = 0;
+  for (int w = tid; w < words; w += kSelThreads) pc += __popc(kept[w]);
   int64_t tot;
-  int64_t run = block_excl_scan<int64_t>(loc, &tot, sm.scan_c);
-  for (int w = wa; w < wb; ++w) {
-    woff[w] = static_cast<int32_t>(run);
-    run += __popc(kept[w]);
-  }
-  __syncthreads();
+  block_excl_scan<int64_t>(pc, &tot, sm.scan_c);
   if (tot != k) {
     leave();
     return;
   }
-  if (base + k <= a.col_capacity) {
-    // a word at a time per warp, lane = bit: each word's keys leave in one
-    // coalesced store whatever their density
-    const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll 4
-    for (int w = warp; w < words; w += kSelWarps) {
-      const uint32_t e = kept[w];
-      if (e != 0u && ((e >> lane) & 1u)) a.col_idx[base + woff[w] + __popc(e & lt)] = w * 32 + lane;
-    }
-  }
+  // ascending emission, staged per warp in the candidates' storage (free now)
+  if (base + k <= a.col_capacity) emit_mask(kept, words, base, a.col_idx, sm.scan_c, sm.cand);
   if (tid == 0) a.counts[row] = k;
 }
 
@@ -2011,7 +2004,7 @@ static TopkPlan plan_topk(const BuildArgs& a, int num_sms) {
     off = align256(off + rows * size_t(nreg) * 4);
     if (off >= region) break;  // (more regions only take more room)
     const int64_t room = static_cast<int64_t>((region - off) / (rows * size_t(nreg) * 8));
-    const int64_t cap = room < kFinCand ? room : kFinCand;
+    const int64_t cap = (room < kFinCand ? room : kFinCand) & ~int64_t(1);  // even: 16-byte pairs
     if (cap < 2.0 * window / nreg + 96) continue;
     const int64_t units = base * ks, waves = (units + num_sms - 1) / num_sms;
     const int64_t cost = waves * ((P.ntiles + ks - 1) / ks + 2);
