@@ -1920,6 +1920,9 @@ static cudaError_t launch_scores(const BuildArgs& a, int num_sms, cudaStream_t s
   s.ntiles = (nkeys + 127) / 128;
   const int64_t base = int64_t(a.BH) * s.gchunks;
   int64_t ks = (2 * int64_t(num_sms) + base - 1) / base;
+  // with a unit filter (a few units flagged) the flagged units' keys are
+  // split finely, so that they spread over the SMs; the rest are skipped
+  if (unit_filter) ks = 64;
   ks = ks < 1 ? 1 : (ks > s.ntiles ? s.ntiles : ks);
   s.tiles_per_split = static_cast<int32_t>((s.ntiles + ks - 1) / ks);
   s.ksplit = (s.ntiles + s.tiles_per_split - 1) / s.tiles_per_split;
