@@ -199,3 +199,11 @@ def test_topk_direct_ties_at_the_cut_by_index():
     check_topk(q, k, 128, 500, rp, col)
     c = col.cpu().numpy().reshape(8, 500)
     assert all(np.array_equal(c[r], np.arange(0, 8000, 16)) for r in range(8))
+
+
+def test_topk_direct_batch_of_two():
+    # B = 2: rows of both batch entries' heads, 192-row groups, d = 64
+    q, k, _ = field(2, 2, 64, (6, 16, 16), (8, 32, 32), seed=11)
+    rp, col, nnz, nf = build_topk(q, k, 192, 777)
+    assert nf == 0
+    check_topk(q, k, 192, 777, rp, col)
