@@ -1354,34 +1354,58 @@ __global__ void __launch_bounds__(RowScoreCfg<D>::kThreads, 1)
           nab += __popc(w[0]) + __popc(w[1]);
           *reinterpret_cast<uint2*>(a.mask + row * a.ld_mask + (j0 >> 5)) = make_uint2(w[0], w[1]);
         }
-        // the candidates' scores leave through the warp's staging area, each
-        // lane walking its own candidate bits
-        if (__any_sync(0xffffffffu, (cw[0] | cw[1]) != 0u)) {
+        // The candidates' scores leave through the warp's staging area, the
+        // whole warp at once: the warp's candidates of this half-tile, row
+        // (lane) by row and key by key, are numbered by a warp scan of the
+        // rows' counts, and lane l takes numbers l, l + 32, ...: it finds the
+        // row holding its number (a binary search over the scan) and the key
+        // (the r-th set bit of that row's word pair).  A row's candidates
+        // fall on consecutive lanes and land in consecutive slots.
+        const int cnt = __popc(cw[0]) + __popc(cw[1]);
+        const int incl = warp_incl_scan(cnt);
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (total > 0) {
           float4* st4 = reinterpret_cast<float4*>(sStage + warp * C::kStage);
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4)
             st4[c4 * 32 + lane] = make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
           __syncwarp();
           const float* st = reinterpret_cast<const float*>(st4);
-          uint64_t cm = (static_cast<uint64_t>(cw[1]) << 32) | cw[0];
-          while (cm) {
-            // two candidates leave in one 16-byte store when the slot is even
-            // (region bases are 16-byte aligned: cap is even)
-            const int c = __ffsll(static_cast<long long>(cm)) - 1;
-            cm &= cm - 1;
-            const uint2 e1 = make_uint2(static_cast<uint32_t>(j0 + c),
-                                        __float_as_uint(st[((c >> 2) * 32 + lane) * 4 + (c & 3)] * a.scale));
-            if ((nc & 1) == 0 && cm != 0ull && nc + 1 < cap) {
-              const int c2 = __ffsll(static_cast<long long>(cm)) - 1;
-              cm &= cm - 1;
-              const uint32_t v2 = __float_as_uint(st[((c2 >> 2) * 32 + lane) * 4 + (c2 & 3)] * a.scale);
-              *reinterpret_cast<uint4*>(cbase + nc) = make_uint4(e1.x, e1.y, static_cast<uint32_t>(j0 + c2), v2);
-              nc += 2;
-            } else {
-              if (nc < cap) cbase[nc] = e1;
-              ++nc;
+          const int excl = incl - cnt;
+          // slot of this row's next candidate, then the row's region start
+          const int first = nc;
+          const int64_t lane_step = int64_t(2) * a.ksplit * cap;  // one row further
+          for (int i0 = 0; i0 < total; i0 += 32) {  // (total is the same in every lane)
+            const int i = i0 + lane;
+            int o = 0;  // the owner: the number of rows whose inclusive count is <= i
+#pragma unroll
+            for (int step = 16; step > 0; step >>= 1)
+              if (__shfl_sync(0xffffffffu, incl, o + step - 1) <= i) o += step;
+            const int r0 = i - __shfl_sync(0xffffffffu, excl, o);
+            const uint32_t m0 = __shfl_sync(0xffffffffu, cw[0], o), m1 = __shfl_sync(0xffffffffu, cw[1], o);
+            const int slot = __shfl_sync(0xffffffffu, first, o) + r0;
+            if (i < total) {
+              // the r-th set bit (0-based) of m1:m0
+              const int p0 = __popc(m0);
+              uint32_t m = r0 < p0 ? m0 : m1;
+              int r = r0 < p0 ? r0 : r0 - p0;
+              int c = r0 < p0 ? 0 : 32;
+#pragma unroll
+              for (int wdt = 16; wdt > 0; wdt >>= 1) {
+                const int p = __popc(m & ((1u << wdt) - 1u));
+                if (r >= p) {
+                  r -= p;
+                  c += wdt;
+                  m >>= wdt;
+                }
+              }
+              if (slot < cap)
+                cbase[int64_t(o - lane) * lane_step + slot] =
+                    make_uint2(static_cast<uint32_t>(j0 + c),
+                               __float_as_uint(st[((c >> 2) * 32 + o) * 4 + (c & 3)] * a.scale));
             }
           }
+          nc += cnt;
           __syncwarp();
         }
       }
@@ -1487,12 +1511,16 @@ done:
 // edge of the bin holding rank r_lo, so at most r_hi samples lie above hi and
 // more than r_lo at or above lo.  A non-finite estimate gives (-inf, inf):
 // every key a candidate.
+// Bin b lives at word b + b / 32 of the warp's histogram: a lane scans 32
+// consecutive bins, and the pad word puts the 32 lanes' reads of one step in 32
+// different banks.
 constexpr int kBrBins = 1024;
 constexpr int kBrWarps = 4;
+__device__ __forceinline__ int br_slot(int b) { return b + (b >> 5); }
 __global__ void __launch_bounds__(32 * kBrWarps) sa_bracket_kernel(const float* samp, int64_t ld_samp,
                                                                     int32_t S, int64_t rows, float r_hi,
                                                                     float r_lo, float2* lohi) {
-  __shared__ uint32_t hist_all[kBrWarps][kBrBins];
+  __shared__ uint32_t hist_all[kBrWarps][kBrBins + kBrBins / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t row = int64_t(blockIdx.x) * kBrWarps + warp;
   if (row >= rows) return;  // warps are independent: no block barrier below
@@ -1529,7 +1557,7 @@ __global__ void __launch_bounds__(32 * kBrWarps) sa_bracket_kernel(const float* 
       mn -= 0.5f * span;
     }
     const float inv = float(kBrBins) / span;
-    for (int i = lane; i < kBrBins; i += 32) hist[i] = 0;
+    for (int i = lane; i < kBrBins + kBrBins / 32; i += 32) hist[i] = 0;
     __syncwarp();
     const int nf4 = S >> 2;
     const float4* x4 = reinterpret_cast<const float4*>(x);
@@ -1545,25 +1573,25 @@ __global__ void __launch_bounds__(32 * kBrWarps) sa_bracket_kernel(const float* 
         const float e[4] = {q4[u].x, q4[u].y, q4[u].z, q4[u].w};
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          if (e[c] == e[c]) atomicAdd(&hist[lin_bin(e[c], mn, inv, kBrBins)], 1u);
+          if (e[c] == e[c]) atomicAdd(&hist[br_slot(lin_bin(e[c], mn, inv, kBrBins))], 1u);
       }
     }
     for (int i = 4 * nf4 + lane; i < S; i += 32) {
       const float v = x[i];
-      if (v == v) atomicAdd(&hist[lin_bin(v, mn, inv, kBrBins)], 1u);
+      if (v == v) atomicAdd(&hist[br_slot(lin_bin(v, mn, inv, kBrBins))], 1u);
     }
     __syncwarp();
     constexpr int per = kBrBins / 32;
     const int top = kBrBins - 1 - per * lane;  // lane 0 holds the highest bins
     uint32_t tot = 0;
 #pragma unroll 8
-    for (int e = 0; e < per; ++e) tot += hist[top - e];
+    for (int e = 0; e < per; ++e) tot += hist[br_slot(top - e)];
     uint32_t c = warp_incl_scan(tot) - tot;  // samples in higher bins
     float hv = INFINITY, lv = -INFINITY;
     bool got_hi = false, got_lo = false;
     for (int e = 0; e < per; ++e) {
       const int bin = top - e;
-      const uint32_t n = hist[bin];
+      const uint32_t n = hist[br_slot(bin)];
       if (n > 0) {
         if (r_hi >= float(c) && r_hi < float(c + n)) {
           got_hi = true;
