@@ -421,6 +421,32 @@ __device__ __forceinline__ float block_min(float v, Sm& sm) {
 }
 template <class Sm>
 __device__ __forceinline__ float block_max(float v, Sm& sm) { return -block_min(-v, sm); }
+// Both at once, with one pair of barriers.
+template <class Sm>
+__device__ __forceinline__ void block_minmax(float* mn, float* mx, Sm& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float a = *mn, b = *mx;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+  __syncthreads();
+  if (lane == 0) {
+    sm.fred[0][warp] = a;
+    sm.fred[1][warp] = b;
+  }
+  __syncthreads();
+  a = sm.fred[0][0];
+  b = sm.fred[1][0];
+#pragma unroll
+  for (int w = 1; w < kSelWarps; ++w) {
+    a = fminf(a, sm.fred[0][w]);
+    b = fmaxf(b, sm.fred[1][w]);
+  }
+  *mn = a;
+  *mx = b;
+}
 
 __device__ __forceinline__ float f4_get(const float4& v, int e) {
   return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
@@ -747,13 +773,19 @@ __device__ void emit_row(const float* s, int Nk, uint32_t ck, int64_t nt, int64_
 __device__ __forceinline__ bool by_mass_mode(const SelArgs& a) { return a.mode != SA_SELECT_TOPK; }
 
 // Writes the indices of the set bits of kept[0, words) in ascending order to
-// col_idx[base, ...).  Warp w owns a contiguous run of words; the runs'
-// offsets come from one block scan of their popcounts.  A warp takes its run
-// 32 words at a time (lane = word): a warp scan of the popcounts places each
-// word's keys in the warp's staging buffer (1024 entries of shared memory),
-// and the pass leaves in coalesced stores.
-__device__ void emit_mask(const uint32_t* kept, int words, int64_t base, int32_t* col_idx,
-                          int64_t* scratch, int32_t* stage_all) {
+// col_idx[base, ...) and returns true, or, when `expect` >= 0 and the number
+// of set bits differs from it, writes nothing and returns false (the same in
+// every thread).  `write` false only counts.  Warp w owns a contiguous run of
+// words; the runs' offsets come from one block scan of their popcounts.  A
+// warp takes its run 32 words at a time (lane = word): a warp scan of the
+// popcounts places each word's keys in the warp's staging buffer (1024 entries
+// of shared memory), and the pass leaves in coalesced stores.  A lane expands
+// its word bit by bit, in 32 fixed predicated steps when some word of the 32
+// has more than 8 keys (a loop over set bits would run as long as the warp's
+// fullest word), else in a loop over its set bits.
+__device__ bool emit_mask(const uint32_t* kept, int words, int64_t base, int32_t* col_idx,
+                          int64_t* scratch, int32_t* stage_all, int64_t expect = -1,
+                          bool write = true) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int per = (words + kSelWarps - 1) / kSelWarps;
   const int w0 = min(words, warp * per), w1 = min(words, w0 + per);
@@ -764,6 +796,8 @@ __device__ void emit_mask(const uint32_t* kept, int words, int64_t base, int32_t
   // block scan over the warps' counts (only lane 0 of each warp contributes)
   int64_t total;
   const int64_t before = block_excl_scan<int64_t>(lane == 0 ? n : 0, &total, scratch);
+  if (expect >= 0 && total != expect) return false;
+  if (!write) return true;
   int64_t pos = base + __shfl_sync(0xffffffffu, before, 0);
   int32_t* stage = stage_all + warp * 1024;
   for (int wb = w0; wb < w1; wb += 32) {
@@ -778,15 +812,23 @@ __device__ void emit_mask(const uint32_t* kept, int words, int64_t base, int32_t
     }
     const int cnt = __shfl_sync(0xffffffffu, x, 31);
     int off = x - c;
-    while (bits) {
-      stage[off++] = w * 32 + (__ffs(bits) - 1);
-      bits &= bits - 1;
+    const int jb = w * 32;
+    if (__reduce_max_sync(0xffffffffu, static_cast<unsigned>(c)) > 8u) {
+#pragma unroll
+      for (int b = 0; b < 32; ++b)
+        if (bits & (1u << b)) stage[off++] = jb + b;
+    } else {
+      while (bits) {
+        stage[off++] = jb + (__ffs(bits) - 1);
+        bits &= bits - 1;
+      }
     }
     __syncwarp();
     for (int i = lane; i < cnt; i += 32) col_idx[pos + i] = stage[i];
     __syncwarp();
     pos += cnt;
   }
+  return true;
 }
 
 // The selection of one score row by the whole block.  TOPK: bit j of
@@ -1726,6 +1768,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const 
     // candidate i of the packed list: region r with reg_off[r] <= i < reg_off[r+1];
     // up to eight loads in flight per thread
     const uint2* src = a.cand + row * int64_t(a.nreg) * a.cap;
+    float wmn = INFINITY, wmx = -INFINITY;
     for (int i0 = 0; i0 < ntot; i0 += 8 * kSelThreads) {
       uint2 e[8];
 #pragma unroll
@@ -1743,18 +1786,15 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const 
       for (int u = 0; u < 8; ++u) {
         const int i = i0 + u * kSelThreads + tid;
         if (i < ntot) {
+          const float xv = __uint_as_float(e[u].y);
           cj[i] = static_cast<int32_t>(e[u].x);
-          cx[i] = __uint_as_float(e[u].y);
+          cx[i] = xv;
+          wmn = fminf(wmn, xv);
+          wmx = fmaxf(wmx, xv);
         }
       }
     }
-    float wmn = INFINITY, wmx = -INFINITY;
-    for (int i = tid; i < ntot; i += kSelThreads) {
-      wmn = fminf(wmn, cx[i]);
-      wmx = fmaxf(wmx, cx[i]);
-    }
-    wmn = block_min(wmn, sm);  // (its barriers also publish cx, cj)
-    wmx = block_max(wmx, sm);
+    block_minmax(&wmn, &wmx, sm);  // (its barriers also publish cx, cj)
     // The need-th candidate by (score descending, key ascending): one
     // histogram over kBins linear bins of [wmn, wmx], the bin where the
     // count from the top reaches need, then an exact ranking of that bin's
@@ -1856,17 +1896,12 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const 
     }
   }
   __syncthreads();
-  // exactly k kept keys, or the row is left to the select kernel
-  int pc = 0;
-  for (int w = tid; w < words; w += kSelThreads) pc += __popc(kept[w]);
-  int64_t tot;
-  block_excl_scan<int64_t>(pc, &tot, sm.scan_c);
-  if (tot != k) {
+  // ascending emission of exactly k kept keys (else the row is left to the
+  // select kernel), staged per warp in the candidates' storage (free now)
+  if (!emit_mask(kept, words, base, a.col_idx, sm.scan_c, sm.cand, k, base + k <= a.col_capacity)) {
     leave();
     return;
   }
-  // ascending emission, staged per warp in the candidates' storage (free now)
-  if (base + k <= a.col_capacity) emit_mask(kept, words, base, a.col_idx, sm.scan_c, sm.cand);
   if (tid == 0) a.counts[row] = k;
 }
 
