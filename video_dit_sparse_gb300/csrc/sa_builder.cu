@@ -1222,8 +1222,8 @@ __global__ void __launch_bounds__(kSelThreads) sa_emit_kernel(const float* score
 // rows, so the lists are exact in every case.
 // Key split ks of a unit takes the key tiles ks, ks + ksplit, ... (spread
 // over the whole sequence, so that every split sees about the same share of
-// a row's candidates however they cluster); each (row, split, half of the
-// tile's columns) has its own candidate region of `cap` slots.
+// a row's candidates however they cluster); each (row, split, 32-column part
+// of the tile) has its own candidate region of `cap` slots.
 struct RowScoreArgs {
   int64_t G, units;
   int32_t Nk, gchunks, ksplit, ntiles;
@@ -1231,22 +1231,24 @@ struct RowScoreArgs {
   const float2* lohi;   // (lo, hi) per row
   uint32_t* mask;       // [rows, ld_mask] words, bit j mod 32 of word j / 32: key j above hi
   int64_t ld_mask;
-  uint2* cand;          // [rows, 2 * ksplit regions, cap]: (key, score bits)
+  uint2* cand;          // [rows, 4 * ksplit regions, cap]: (key, score bits)
   int32_t cap;
-  int32_t* nabove;      // [rows, 2 * ksplit]: keys above hi
-  int32_t* ncand;       // [rows, 2 * ksplit]: keys in [lo, hi] (may exceed cap)
+  int32_t* nabove;      // [rows, 4 * ksplit]: keys above hi
+  int32_t* ncand;       // [rows, 4 * ksplit]: keys in [lo, hi] (may exceed cap)
   int32_t* status;
 };
 
 template <int D>
 struct RowScoreCfg {
   static constexpr int kStages = 3;
-  static constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, 64 key columns each
+  // four per TMEM lane quarter, one 32-key column part of the tile each
+  static constexpr int kParts = 4;
+  static constexpr int kEpiWarps = 4 * kParts;
   static constexpr int kMmaWarp = kEpiWarps, kTmaWarp = kEpiWarps + 1;
   static constexpr int kThreads = 32 * (kEpiWarps + 2);
   static constexpr int kTile = 128 * D * 2;  // 128 rows of d bf16
-  // each epilogue warp stages its 32 rows x 64 raw scores, [c / 4][lane] float4s
-  static constexpr int kStage = 32 * 64 * 4;
+  // each epilogue warp stages its 32 rows x 32 raw scores, [c / 4][lane] float4s
+  static constexpr int kStage = 32 * 32 * 4;
   static constexpr int kSmemBytes = 1024 + 2 * kTile + kStages * kTile + kEpiWarps * kStage + 1024;
   static constexpr int kTmemCols = 256;      // two 128-column accumulators
 };
@@ -1322,8 +1324,10 @@ __global__ void __launch_bounds__(RowScoreCfg<D>::kThreads, 1)
 
   if (warp < C::kEpiWarps) {
     // ------------------------------------------------------------ epilogue
-    // Thread = one mean-query row (TMEM lane), 64 key columns of each tile.
-    const int quarter = warp & 3, half = warp >> 2;
+    // Thread = one mean-query row (TMEM lane), 32 key columns of each tile.
+    // Four warps share a lane quarter, so that a sub-partition has four
+    // epilogue warps to hide the latency of each one's chain of steps.
+    const int quarter = warp & 3, part = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const int gi = quarter * 32 + lane;
     uint32_t t = 0;
@@ -1334,7 +1338,7 @@ __global__ void __launch_bounds__(RowScoreCfg<D>::kThreads, 1)
       const int64_t g = int64_t(gc) * 128 + gi;
       const bool valid = g < a.G;
       const int64_t row = bh * a.G + g;
-      const int64_t region = (row * a.ksplit + ks) * 2 + half;
+      const int64_t region = (row * a.ksplit + ks) * C::kParts + part;
       // scale > 0: scale*x > hi <=> x > xa and scale*x < lo <=> x < xb, with
       // xa the largest x whose rounded score is <= hi, xb the smallest whose
       // rounded score is >= lo (found from the quotients by stepping ulps)
@@ -1346,6 +1350,7 @@ __global__ void __launch_bounds__(RowScoreCfg<D>::kThreads, 1)
       }
       uint2* cbase = a.cand + region * a.cap;
       const int cap = a.cap;
+      const int64_t lane_step = int64_t(C::kParts) * a.ksplit * cap;  // one row further
       int nab = 0, nc = 0;
       for (int tile = ks; tile < a.ntiles; tile += a.ksplit, ++t) {
         const uint32_t b = t & 1;
@@ -1353,85 +1358,67 @@ __global__ void __launch_bounds__(RowScoreCfg<D>::kThreads, 1)
         const bool got = mbar_wait(&bars->dfull[b], (t >> 1) & 1, abort);
         if (!__all_sync(0xffffffffu, got)) goto done;
         tc_fence_after();
-        float x[64];
-        const uint32_t src = tmem + lane_base + b * 128 + half * 64;
-        tmem_ld32(src, reinterpret_cast<uint32_t*>(x));
-        tmem_ld32(src + 32, reinterpret_cast<uint32_t*>(x + 32));
+        float x[32];
+        tmem_ld32(tmem + lane_base + b * 128 + part * 32, reinterpret_cast<uint32_t*>(x));
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->dempty[b]);
         // (rows past G take part in the warp's collective steps with no keys)
-        const int j0 = tile * 128 + half * 64;
+        const int j0 = tile * 128 + part * 32;
         // key c is above when xa - x < 0 and below when x - xb < 0 (for floats
         // p != q, p - q is never zero; xa is never -0 and xb never +0): the
-        // sign bits are funnel-shifted into words, highest key first, in
-        // four chains of 16 keys per word
-        uint32_t w[2], bl[2];
+        // sign bits are funnel-shifted into a word, highest key first, in
+        // four chains of 16 keys
+        uint32_t a0 = 0u, a1 = 0u, b0 = 0u, b1 = 0u;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t a0 = 0u, a1 = 0u, b0 = 0u, b1 = 0u;
-#pragma unroll
-          for (int c = 15; c >= 0; --c) {
-            a0 = shl_in(a0, __float_as_uint(xa - x[32 * h + c]));
-            a1 = shl_in(a1, __float_as_uint(xa - x[32 * h + 16 + c]));
-            b0 = shl_in(b0, __float_as_uint(x[32 * h + c] - xb));
-            b1 = shl_in(b1, __float_as_uint(x[32 * h + 16 + c] - xb));
-          }
-          w[h] = (a1 << 16) | a0;
-          bl[h] = (b1 << 16) | b0;
+        for (int c = 15; c >= 0; --c) {
+          a0 = shl_in(a0, __float_as_uint(xa - x[c]));
+          a1 = shl_in(a1, __float_as_uint(xa - x[16 + c]));
+          b0 = shl_in(b0, __float_as_uint(x[c] - xb));
+          b1 = shl_in(b1, __float_as_uint(x[16 + c] - xb));
         }
-        uint32_t cw[2] = {~(w[0] | bl[0]), ~(w[1] | bl[1])};  // neither above nor below
-        if (j0 + 64 > a.Nk || !valid) {
-          const int rem = valid ? a.Nk - j0 : 0;  // keys of this half that exist
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int r = rem - 32 * h;
-            const uint32_t keep = r >= 32 ? 0xFFFFFFFFu : (r <= 0 ? 0u : (1u << r) - 1u);
-            w[h] &= keep;
-            cw[h] &= keep;
-          }
+        uint32_t w = (a1 << 16) | a0;
+        uint32_t cw = ~(w | (b1 << 16) | b0);  // neither above nor below
+        if (j0 + 32 > a.Nk || !valid) {
+          const int r = valid ? a.Nk - j0 : 0;  // keys of this part that exist
+          const uint32_t keep = r >= 32 ? 0xFFFFFFFFu : (r <= 0 ? 0u : (1u << r) - 1u);
+          w &= keep;
+          cw &= keep;
         }
         if (valid) {
-          nab += __popc(w[0]) + __popc(w[1]);
-          *reinterpret_cast<uint2*>(a.mask + row * a.ld_mask + (j0 >> 5)) = make_uint2(w[0], w[1]);
+          nab += __popc(w);
+          a.mask[row * a.ld_mask + (j0 >> 5)] = w;
         }
         // The candidates' scores leave through the warp's staging area, the
-        // whole warp at once: the warp's candidates of this half-tile, row
-        // (lane) by row and key by key, are numbered by a warp scan of the
-        // rows' counts, and lane l takes numbers l, l + 32, ...: it finds the
-        // row holding its number (a binary search over the scan) and the key
-        // (the r-th set bit of that row's word pair).  A row's candidates
-        // fall on consecutive lanes and land in consecutive slots.
-        const int cnt = __popc(cw[0]) + __popc(cw[1]);
+        // whole warp at once: the warp's candidates of this part, row (lane)
+        // by row and key by key, are numbered by a warp scan of the rows'
+        // counts, and lane l takes numbers l, l + 32, ...: it finds the row
+        // holding its number (a binary search over the scan) and the key (the
+        // r-th set bit of that row's word).  A row's candidates fall on
+        // consecutive lanes and land in consecutive slots.
+        const int cnt = __popc(cw);
         const int incl = warp_incl_scan(cnt);
         const int total = __shfl_sync(0xffffffffu, incl, 31);
         if (total > 0) {
           float4* st4 = reinterpret_cast<float4*>(sStage + warp * C::kStage);
 #pragma unroll
-          for (int c4 = 0; c4 < 16; ++c4)
+          for (int c4 = 0; c4 < 8; ++c4)
             st4[c4 * 32 + lane] = make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
           __syncwarp();
           const float* st = reinterpret_cast<const float*>(st4);
           const int excl = incl - cnt;
-          // slot of this row's next candidate, then the row's region start
-          const int first = nc;
-          const int64_t lane_step = int64_t(2) * a.ksplit * cap;  // one row further
           for (int i0 = 0; i0 < total; i0 += 32) {  // (total is the same in every lane)
             const int i = i0 + lane;
             int o = 0;  // the owner: the number of rows whose inclusive count is <= i
 #pragma unroll
             for (int step = 16; step > 0; step >>= 1)
               if (__shfl_sync(0xffffffffu, incl, o + step - 1) <= i) o += step;
-            const int r0 = i - __shfl_sync(0xffffffffu, excl, o);
-            const uint32_t m0 = __shfl_sync(0xffffffffu, cw[0], o), m1 = __shfl_sync(0xffffffffu, cw[1], o);
-            const int slot = __shfl_sync(0xffffffffu, first, o) + r0;
+            int r = i - __shfl_sync(0xffffffffu, excl, o);
+            uint32_t m = __shfl_sync(0xffffffffu, cw, o);
+            const int slot = __shfl_sync(0xffffffffu, nc, o) + r;
             if (i < total) {
-              // the r-th set bit (0-based) of m1:m0
-              const int p0 = __popc(m0);
-              uint32_t m = r0 < p0 ? m0 : m1;
-              int r = r0 < p0 ? r0 : r0 - p0;
-              int c = r0 < p0 ? 0 : 32;
+              int c = 0;  // the r-th set bit (0-based) of m
 #pragma unroll
               for (int wdt = 16; wdt > 0; wdt >>= 1) {
                 const int p = __popc(m & ((1u << wdt) - 1u));
@@ -2048,15 +2035,15 @@ static TopkPlan plan_topk(const BuildArgs& a, int num_sms) {
   // the row's mask in shared memory, its word offsets in the window storage
   if (kFinMaskOff + size_t(P.ld_mask) * 4 > 160 * 1024 || P.ld_mask > 2 * kFinCand) return P;
   const size_t rows = size_t(a.rows), region = rows * size_t(a.L.ld) * 4;
-  // Key splits: among the counts (at most 32, so at most 64 candidate regions
+  // Key splits: among the counts (at most 16, so at most 64 candidate regions
   // per row) whose regions fit the scores region, the one that minimises the
   // tiles of the busiest SM, counting two tiles of start-up per unit.  A
   // region takes what the scores region holds, up to kFinCand slots; its
   // expected share of the bracket (tiles spread over the sequence) must fit
   // twice over, plus 96.
   int64_t best = -1;
-  for (int ks = 1; ks <= 32 && ks <= P.ntiles; ++ks) {
-    const int nreg = 2 * ks;
+  for (int ks = 1; ks <= 16 && ks <= P.ntiles; ++ks) {
+    const int nreg = 4 * ks;
     size_t off = 0;
     const size_t samp = off;
     off = align256(off + rows * size_t(P.ld_samp) * 4);
