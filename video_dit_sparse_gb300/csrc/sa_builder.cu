@@ -2057,7 +2057,7 @@ static TopkPlan plan_topk(const BuildArgs& a, int num_sms) {
     off = align256(off + rows * size_t(nreg) * 4);
     if (off >= region) break;  // (more regions only take more room)
     const int64_t room = static_cast<int64_t>((region - off) / (rows * size_t(nreg) * 8));
-    const int64_t cap = (room < kFinCand ? room : kFinCand) & ~int64_t(1);  // even: 16-byte pairs
+    const int64_t cap = (room < kFinCand ? room : kFinCand) & ~int64_t(1);  // (even: every region starts 16-byte aligned)
     if (cap < 2.0 * window / nreg + 96) continue;
     const int64_t units = base * ks, waves = (units + num_sms - 1) / num_sms;
     const int64_t cost = waves * ((P.ntiles + ks - 1) / ks + 2);
