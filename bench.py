@@ -97,6 +97,25 @@ def kept_pairs(row_ptr: np.ndarray, B, H, Nq, M) -> int:
     return int((counts * rows[None, :]).sum())
 
 
+def builder_and_gather(B, H, Nq, Nk, d, M, nnz, ms_build, ms_fwd, hbm_gbs, peak_kind):
+    """The index builder against the HBM roofline, and the rate of the
+    forward's gather.  The builder's algorithmic bytes are one read of Q and
+    K (2·d bytes per token row) and the lists it writes (4 bytes per kept
+    index, 8 per row offset); the gather moves 4·d bytes (one K and one V row)
+    per (group, kept key) from L2 into shared memory inside the forward
+    kernel, so it has no DRAM roofline of its own."""
+    rows = B * H * (-(-Nq // M))
+    build_bytes = 2 * d * (Nq + Nk) * B * H + 4 * nnz + 8 * (rows + 1)
+    gbs = build_bytes / (ms_build * 1e-3) / 1e9
+    builder = {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s",
+               "frac": gbs / hbm_gbs, "bytes_per_step": int(build_bytes), "ms": ms_build,
+               "peak_source": f"{peak_kind} hbm_gbs"}
+    gather_bytes = 4 * d * nnz
+    gather = {"source": "L2", "achieved": gather_bytes / (ms_fwd * 1e-3) / 1e9, "unit": "GB/s",
+              "bytes_per_step": int(gather_bytes)}
+    return builder, gather
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -366,13 +385,15 @@ def run_ours(args, w):
                 "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
                 "kernel": "sa_forward_kernel", "peak_source": f"{pk_kind} bf16_tflops (burst)",
                 "frac_of_sustained": achieved / pk.get("bf16_tflops_sustained", pk["bf16_tflops"])}
+    builder, gather = builder_and_gather(w.B, w.H, w.Nq, w.Nk, w.d, w.group, int(nnz_now()),
+                                         float(np.mean(t_build)), fwd_ms, pk["hbm_gbs"], pk_kind)
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": workload_config(w, pairs),
             "ms_build_index": float(np.mean(t_build)), "ms_forward": fwd_ms,
             "gpu_launches": kernels_per_step(w.mode, w.topk, w.Nk) * args.steps,
-            "roofline": roofline,
+            "roofline": roofline, "builder": builder, "gather": gather,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": int(3 * q.numel() * 2),
                     "d2h_bytes_per_step": int(o.numel() * 2 + lse.numel() * 4),

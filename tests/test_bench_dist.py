@@ -50,3 +50,21 @@ def test_kept_pairs_counts_ragged_groups():
     counts = np.array([5, 6, 7, 1, 2, 3])
     row_ptr = np.concatenate([[0], np.cumsum(counts)])
     assert bench.kept_pairs(row_ptr, 1, 2, 300, 128) == 128 * (5 + 6 + 1 + 2) + 44 * (7 + 3)
+
+
+def test_builder_and_gather_bytes():
+    import bench
+    # 24 heads x 16384 tokens, d = 128, groups of 128, 3277 keys per group
+    rows = 24 * 128
+    nnz = rows * 3277
+    b, g = bench.builder_and_gather(1, 24, 16384, 16384, 128, 128, nnz, 0.2, 0.6, 6781.8, "measured")
+    qk = 2 * 128 * (16384 + 16384) * 24  # Q and K read once: 201.3 MB
+    assert b["bytes_per_step"] == qk + 4 * nnz + 8 * (rows + 1)
+    assert abs(b["bytes_per_step"] - 241.6e6) < 0.1e6
+    assert abs(b["achieved"] - b["bytes_per_step"] / 0.2e-3 / 1e9) < 1e-6
+    assert abs(b["frac"] - b["achieved"] / 6781.8) < 1e-12 and b["unit"] == "GB/s"
+    assert g["bytes_per_step"] == 4 * 128 * nnz  # 5.15 GB: one K and one V row per kept key
+    assert abs(g["achieved"] - 4 * 128 * nnz / 0.6e-3 / 1e9) < 1e-6
+    # a ragged last group still counts as one row of lists
+    b2, _ = bench.builder_and_gather(2, 3, 300, 1000, 64, 128, 10, 1.0, 1.0, 1.0, "fallback")
+    assert b2["bytes_per_step"] == 2 * 64 * 1300 * 6 + 40 + 8 * (2 * 3 * 3 + 1)
