@@ -10,8 +10,17 @@ HBM; `e2e` is the same metric with host buffers (H2D of q, k, v and D2H of
 o, lse inside the timed region); `roofline` is the forward kernel against
 the measured bf16 tensor peak.  `--impl reference` times the fp64 CPU
 oracle on a bounded sample of the same workload.
-Under torchrun (N > 1) every rank runs the full layer on its own GPU (weak
-scaling; heads are independent, no collective on the data path).
+
+The default workload is the 69K-token density sweep at 20 % (24 heads,
+18x48x80 latent grid in (2,8,8) voxels, M = 128, top 13824 keys per group).
+
+Under torchrun (N > 1) the (batch, head) units are independent, so no
+collective touches the data path:
+  --split batch (default): rank r runs its own layer (batch element r, seeded
+                 r): weak scaling, per-GPU work fixed;
+  --split heads: rank r runs heads [r*H/N, (r+1)*H/N) of one layer: strong
+                 scaling, total work fixed.
+Rank 0 reports the slowest rank's step time and the work of all ranks.
 """
 from __future__ import annotations
 
@@ -32,7 +41,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "effective TFLOP/s on kept scores (4·d/pair) & ms/layer; % of GB300 dense BF16 TC peak"
-DEFAULT_WORKLOAD = "wan16k_top20"
+DEFAULT_WORKLOAD = "sweep69k_top20"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
 
@@ -181,6 +190,33 @@ def dist_info():
     return world, rank, local
 
 
+def partition_heads(H: int, world: int, rank: int):
+    """Heads [h0, h1) of rank `rank` when one layer's H heads are split over
+    `world` ranks: contiguous and as even as possible (sizes differ by at
+    most one)."""
+    if world < 1 or not 0 <= rank < world or world > H:
+        raise ValueError(f"cannot split {H} heads over {world} ranks")
+    return rank * H // world, (rank + 1) * H // world
+
+
+def local_workload(w, split: str, world: int, rank: int):
+    """(workload of this rank, input seed, head range or None)."""
+    import dataclasses
+    if world == 1:
+        return w, 0, None
+    if split == "heads":
+        h0, h1 = partition_heads(w.H, world, rank)
+        return dataclasses.replace(w, H=h1 - h0), 0, (h0, h1)
+    return w, rank, None
+
+
+def slice_heads(x: dict, heads):
+    if heads is None:
+        return x
+    h0, h1 = heads
+    return {n: np.ascontiguousarray(a[:, h0:h1]) for n, a in x.items() if n in ("q", "k", "v")}
+
+
 def aggregate(local_ms: float, local_units: float, world: int, group=None):
     """Max step time over ranks and total units (all-reduce on the host
     backend; the only collective in the benchmark)."""
@@ -253,7 +289,7 @@ def run_reference(args, w):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(w, None),
+            "data": "synthetic", "config": workload_config(w, topk_pairs(w), args.split, args.gpus),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -261,7 +297,15 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(w, pairs):
+def topk_pairs(w):
+    """Kept pairs of a TOPK layer, known without running it: every group keeps
+    min(k, Nk) keys for each of its rows.  None for data-dependent rules."""
+    if w.mode != "topk":
+        return None
+    return w.B * w.H * w.Nq * min(w.topk, w.Nk)
+
+
+def workload_config(w, pairs, split="batch", world=1):
     c = {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
          "group": w.group, "selection": {"topk": f"k={w.topk}", "mass": f"rho={w.mass}",
                                          "threshold": f"tau={w.threshold}",
@@ -270,6 +314,8 @@ def workload_config(w, pairs):
          "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)"}
     if pairs is not None:
         c["kept_pairs"] = pairs
+    if world > 1:
+        c["parallelism"] = f"{split} split over {world} ranks"
     return c
 
 
@@ -284,7 +330,9 @@ def run_ours(args, w):
     from video_dit_sparse_gb300 import binding as sa
     from video_dit_sparse_gb300 import inputs as I
 
-    x = I.make_inputs(w, 0)
+    w_layer = w
+    w, seed, heads = local_workload(w, args.split, world, rank)
+    x = slice_heads(I.make_inputs(w_layer if heads else w, seed), heads)
     dev = torch.device("cuda", local)
 
     def host(b):
@@ -330,6 +378,7 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     pairs = kept_pairs(row_ptr.cpu().numpy(), w.B, w.H, w.Nq, w.group)
     flops = 4.0 * w.d * pairs
+    _, pairs_total = aggregate(0.0, float(pairs), world)
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if world > 1:
@@ -389,8 +438,11 @@ def run_ours(args, w):
                                          float(np.mean(t_build)), fwd_ms, pk["hbm_gbs"], pk_kind)
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": workload_config(w, pairs),
+            "higher_is_better": True,
+            "scaling": "strong" if (world > 1 and args.split == "heads") else "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w_layer if heads else w,
+                                      int(pairs_total) if heads else pairs, args.split, world),
             "ms_build_index": float(np.mean(t_build)), "ms_forward": fwd_ms,
             "gpu_launches": kernels_per_step(w.mode, w.topk, w.Nk) * args.steps,
             "roofline": roofline, "builder": builder, "gather": gather,
@@ -685,6 +737,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
                     help="run the workload with this many heads (smaller ncu captures)")
+    ap.add_argument("--split", choices=["batch", "heads"], default="batch",
+                    help="N > 1: each rank its own layer (batch) or a share of one layer's heads")
     args = ap.parse_args()
     from video_dit_sparse_gb300 import inputs as I
     w = I.preset(args.workload)

@@ -165,9 +165,12 @@ sa_status sparse_attn_build_index(const sa_problem* problem, const sa_select* se
  * device array of SA_NOALLOC_WORKSPACE_BYTES (32 MiB), which every GPU that
  * loads this code holds until the process exits.  A problem whose
  * sparse_attn_build_index_workspace_size exceeds that returns
- * SA_ERR_UNSUPPORTED before anything is enqueued.  The first call on each
- * device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.
+ * SA_ERR_UNSUPPORTED before anything is enqueued.  Each CUDA context on a
+ * device holds its own instance of the array: the first call in a context
+ * (for most callers, the device's primary context) looks up its device
+ * address (cudaGetSymbolAddress) with that context current, and a call from
+ * another context looks it up again; make the first call in each context
+ * before any stream capture.
  * Every call shares the array and leaves its contents behind: calls that
  * overlap on the GPU (other streams, other host threads) race on it and must
  * be serialised by the caller.  Calls no allocating function.

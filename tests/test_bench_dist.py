@@ -1,7 +1,9 @@
-"""The benchmark's multi-rank path on CPU: world size 2 over gloo.  Each
-rank runs the whole layer on its own GPU in the real benchmark (heads are
-independent: no data exchange); the only collective is the max-over-ranks
-step time and the sum of the work, checked here without a GPU."""
+"""The benchmark's multi-rank path on CPU: world size 2 over gloo.  In the
+real benchmark each rank runs its own layer (--split batch) or a share of one
+layer's heads (--split heads) on its own GPU; heads are independent, so there
+is no data exchange.  The only collective is the max-over-ranks step time and
+the sum of the work, checked here without a GPU, together with the head
+partition."""
 import os
 import socket
 
@@ -68,3 +70,53 @@ def test_builder_and_gather_bytes():
     # a ragged last group still counts as one row of lists
     b2, _ = bench.builder_and_gather(2, 3, 300, 1000, 64, 128, 10, 1.0, 1.0, 1.0, "fallback")
     assert b2["bytes_per_step"] == 2 * 64 * 1300 * 6 + 40 + 8 * (2 * 3 * 3 + 1)
+
+
+def _heads_rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    from video_dit_sparse_gb300 import inputs as I
+    w = I.preset("sweep69k_top20")
+    lw, seed, heads = bench.local_workload(w, "heads", world, rank)
+    # each rank's share of the layer's work, summed by the benchmark's reduction
+    _, pairs_total = bench.aggregate(float(rank), float(bench.topk_pairs(lw)), world)
+    shares = [None] * world
+    dist.all_gather_object(shares, heads)
+    q.put((rank, lw.H, seed, heads, shares, pairs_total, bench.topk_pairs(w)))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_head_split_covers_every_head_once(world):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_heads_rank, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(world))
+    heads = [h for _, _, _, h, _, _, _ in got]
+    covered = sorted(i for h0, h1 in heads for i in range(h0, h1))
+    assert covered == list(range(24))  # every head exactly once
+    for rank, H, seed, (h0, h1), shares, pairs_total, pairs_layer in got:
+        assert H == h1 - h0 and seed == 0 and abs(H - 24 / world) < 1
+        assert shares == heads  # every rank agrees on the partition
+        assert pairs_total == pairs_layer  # the units add up to the whole layer
+
+
+def test_partition_heads_rules():
+    import bench
+    assert [bench.partition_heads(24, 5, r) for r in range(5)] == [(0, 4), (4, 9), (9, 14), (14, 19), (19, 24)]
+    assert bench.partition_heads(12, 1, 0) == (0, 12)
+    with pytest.raises(ValueError):
+        bench.partition_heads(2, 3, 0)  # more ranks than heads
+    from video_dit_sparse_gb300 import inputs as I
+    w = I.preset("wan16k_top20")
+    assert bench.local_workload(w, "batch", 4, 3) == (w, 3, None)  # own layer, own seed
+    assert bench.topk_pairs(w) == 24 * 16384 * 3277
+    assert bench.topk_pairs(I.preset("rollingkv_mass99")) is None

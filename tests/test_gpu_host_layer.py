@@ -47,3 +47,26 @@ def test_host_layer_rejects_short_capacity():
     with pytest.raises(sa.SparseAttnError) as e:
         layer(z, z, z, z.clone(), l)
     assert e.value.status == sa.SA_ERR_CAPACITY
+
+
+def test_host_layer_checks_staging_buffers_before_any_copy():
+    """An undersized device staging buffer is refused before the first copy
+    is enqueued: nothing is written to it or to the host output."""
+    from video_dit_sparse_gb300 import binding as sa
+    B, H, N, d = 1, 24, 16384, 128  # 96 MiB per tensor
+    layer = sa.HostLayer(B, H, N, N, d, group_size=128, mode="topk", topk=64, heads_per_chunk=4)
+    torch.cuda.synchronize()
+    # 2 MiB in a fresh allocation segment (no cached block to carve it from),
+    # far smaller than the 96 MiB q needs
+    torch.cuda.empty_cache()
+    small = torch.full((1, 1, 8192, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    layer.q = small
+    z = torch.zeros(B, H, N, d, dtype=torch.bfloat16)
+    o_h = torch.full((B, H, N, d), 3.0, dtype=torch.bfloat16)
+    l_h = torch.full((B, H, N), 5.0, dtype=torch.float32)
+    with pytest.raises(sa.SparseAttnError) as e:
+        layer(z, z, z, o_h, l_h)
+    assert e.value.status == sa.SA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert bool((layer.q == 7.0).all())
+    assert bool((o_h == 3.0).all()) and bool((l_h == 5.0).all())

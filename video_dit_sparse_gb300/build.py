@@ -75,7 +75,7 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
             sys.stderr.write(log)
     if force or todo or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [exe] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
+        cmd = [exe] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static", "-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -3,6 +3,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -12,12 +14,18 @@
 
 namespace {
 
-constexpr int32_t kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int32_t kVersion = 1 * 10000 + 1 * 100 + 0;
 constexpr int kMaxDevices = 64;
 
-struct Dims {
-  int64_t G, rows;
-};
+std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_ok[kMaxDevices];  // 0 unknown, 1 sm_103, 2 other
+
+using AddrRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+std::atomic<AddrRangeFn> g_addr_range{nullptr};
+
+}  // namespace
+
+namespace sa {
 
 sa_status check_problem(const sa_problem* p, Dims* dims) {
   if (!p) return SA_ERR_INVALID_ARG;
@@ -36,14 +44,18 @@ sa_status check_problem(const sa_problem* p, Dims* dims) {
   return SA_OK;
 }
 
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// --------------------------------------------------------------- device info
-std::atomic<int> g_sms[kMaxDevices];
-std::atomic<int> g_ok[kMaxDevices];  // 0 unknown, 1 sm_103, 2 other
-
-using AddrRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
-std::atomic<AddrRangeFn> g_addr_range{nullptr};
+sa_status check_select(const sa_problem* p, const sa_select* sel, int32_t stat) {
+  if (!sel || sel->mode < SA_SELECT_TOPK || sel->mode > SA_SELECT_MASS) return SA_ERR_INVALID_ARG;
+  if (sel->mode == SA_SELECT_TOPK && sel->topk < 1) return SA_ERR_INVALID_ARG;
+  if (sel->mode == SA_SELECT_THRESHOLD) {
+    // a probability for the mean-query rule and the column maximum; a column
+    // sum can reach the group's row count
+    const double tmax = stat == 1 ? double(p->group_size) : 1.0;
+    if (!(sel->threshold >= 0.0 && sel->threshold <= tmax)) return SA_ERR_INVALID_ARG;
+  }
+  if (sel->mode == SA_SELECT_MASS && !(sel->mass > 0.0 && sel->mass <= 1.0)) return SA_ERR_INVALID_ARG;
+  return SA_OK;
+}
 
 sa_status device_info(int* num_sms) {
   int dev = 0;
@@ -52,7 +64,7 @@ sa_status device_info(int* num_sms) {
   int ok = g_ok[dev].load();
   if (ok == 0) {
     int major = 0, minor = 0, sms = 0;
-    if (cudaFree(nullptr) != cudaSuccess ||  // makes the primary context current
+    if (cudaFree(nullptr) != cudaSuccess ||  // makes a context current (the primary one if none is)
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -75,17 +87,105 @@ sa_status device_info(int* num_sms) {
   return SA_OK;
 }
 
-// [p, p + bytes) must lie inside one device allocation.  Catches host
-// pointers, freed memory and buffers too small for the stated shape before
-// any kernel could touch them.
+// Catches host pointers, freed memory and buffers too small for the stated
+// shape before any kernel could touch them.  device_info() resolves the
+// query first.
 bool in_device_allocation(const void* p, uint64_t bytes) {
   if (!p) return false;
+  const AddrRangeFn fn = g_addr_range.load();
+  if (!fn) return false;
   CUdeviceptr base = 0;
   size_t size = 0;
   const CUdeviceptr dp = reinterpret_cast<CUdeviceptr>(p);
-  if (g_addr_range.load()(&base, &size, dp) != CUDA_SUCCESS) return false;
+  if (fn(&base, &size, dp) != CUDA_SUCCESS) return false;
   return dp >= base && bytes <= size && dp - base <= size - bytes;
 }
+
+NvtxRange::NvtxRange(const char* name) { nvtxRangePushA(name); }
+NvtxRange::~NvtxRange() { nvtxRangePop(); }
+
+sa_status prepare_build(const sa_problem* p, const sa_select* sel, int32_t stat, const void* q,
+                        const void* k, const float* lse, int64_t* row_ptr, int32_t* col_idx,
+                        int64_t col_capacity, int64_t* nnz_out_host, size_t scratch_bytes,
+                        sa_status scratch_short, BuildArgs* a, int* num_sms) {
+  Dims dims;
+  sa_status st = check_problem(p, &dims);
+  if (st != SA_OK) return st;
+  if ((st = check_select(p, sel, stat)) != SA_OK) return st;
+  if (!q || !k || !row_ptr || col_capacity < 0) return SA_ERR_INVALID_ARG;
+  if (stat >= 0 && (!lse || !aligned(lse, 4))) return SA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(row_ptr, 8) || (col_idx && !aligned(col_idx, 4)))
+    return SA_ERR_INVALID_ARG;
+  const BuildLayout L = build_layout(dims.rows, p->Nk, p->d);
+  if (scratch_bytes < L.total) return scratch_short;
+  const int64_t max_nnz = dims.rows * p->Nk;
+  if (sel->mode == SA_SELECT_TOPK) {
+    const int64_t kk = sel->topk < p->Nk ? sel->topk : p->Nk;
+    if (dims.rows * kk > col_capacity) {
+      if (nnz_out_host) *nnz_out_host = dims.rows * kk;
+      return SA_ERR_CAPACITY;
+    }
+  } else if (col_capacity < max_nnz && !nnz_out_host) {
+    return SA_ERR_INVALID_ARG;  // data-dependent nnz needs the synchronous report
+  }
+  if (col_capacity > 0 && !col_idx) return SA_ERR_INVALID_ARG;
+  if ((st = device_info(num_sms)) != SA_OK) return st;
+  const uint64_t qbytes = uint64_t(p->B) * p->H * p->Nq * p->d * 2;
+  const uint64_t kbytes = uint64_t(p->B) * p->H * p->Nk * p->d * 2;
+  if (!in_device_allocation(q, qbytes) || !in_device_allocation(k, kbytes) ||
+      !in_device_allocation(row_ptr, uint64_t(dims.rows + 1) * 8) ||
+      (stat >= 0 && !in_device_allocation(lse, uint64_t(p->B) * p->H * p->Nq * 4)) ||
+      (col_capacity > 0 && !in_device_allocation(col_idx, uint64_t(col_capacity) * 4)))
+    return SA_ERR_INVALID_ARG;
+  a->q = static_cast<const uint16_t*>(q);
+  a->k = static_cast<const uint16_t*>(k);
+  a->lse = lse;
+  a->stat = stat;
+  a->row_ptr = row_ptr;
+  a->col_idx = col_idx;
+  a->col_capacity = col_capacity;
+  a->ws = nullptr;
+  a->L = L;
+  a->rows = dims.rows;
+  a->G = dims.G;
+  a->BH = p->B * p->H;
+  a->Nq = p->Nq;
+  a->Nk = p->Nk;
+  a->d = p->d;
+  a->M = p->group_size;
+  a->scale = p->scale;
+  a->mode = sel->mode;
+  a->topk = sel->topk;
+  a->threshold = sel->threshold;
+  a->mass = sel->mass;
+  return SA_OK;
+}
+
+sa_status run_build(const BuildArgs& a, int num_sms, int64_t* nnz_out_host, cudaStream_t s) {
+  NvtxRange range("sparse_attn_build_index");
+  if (launch_build_index(a, num_sms, s) != cudaSuccess) return SA_ERR_CUDA;
+  if (nnz_out_host) {
+    int64_t misc[2] = {0, 0};
+    if (cudaMemcpyAsync(misc, a.ws + a.L.misc, sizeof misc, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return SA_ERR_CUDA;
+    *nnz_out_host = misc[0];
+    const int32_t dev_status = static_cast<int32_t>(misc[1] & 0xFFFFFFFF);
+    if (dev_status & SA_DEVERR_TIMEOUT) return SA_ERR_TIMEOUT;
+    if (dev_status & SA_DEVERR_CAPACITY) return SA_ERR_CAPACITY;
+  }
+  return SA_OK;
+}
+
+}  // namespace sa
+
+namespace {
+
+using sa::aligned;
+using sa::check_problem;
+using sa::device_info;
+using sa::Dims;
+using sa::in_device_allocation;
 
 sa_status map_cuda(cudaError_t e) { return e == cudaSuccess ? SA_OK : SA_ERR_CUDA; }
 
@@ -125,82 +225,15 @@ sa_status build_common(const sa_problem* p, const sa_select* sel, int32_t stat, 
                        const void* k, const float* lse, int64_t* row_ptr, int32_t* col_idx,
                        int64_t col_capacity, int64_t* nnz_out_host, void* workspace,
                        size_t workspace_bytes, sa_stream_t stream) {
-  Dims dims;
-  sa_status st = check_problem(p, &dims);
-  if (st != SA_OK) return st;
-  if (!sel || sel->mode < SA_SELECT_TOPK || sel->mode > SA_SELECT_MASS) return SA_ERR_INVALID_ARG;
-  if (sel->mode == SA_SELECT_TOPK && sel->topk < 1) return SA_ERR_INVALID_ARG;
-  if (sel->mode == SA_SELECT_THRESHOLD) {
-    // a probability for the mean-query rule and the column maximum; a column
-    // sum can reach the group's row count
-    const double tmax = stat == 1 ? double(p->group_size) : 1.0;
-    if (!(sel->threshold >= 0.0 && sel->threshold <= tmax)) return SA_ERR_INVALID_ARG;
-  }
-  if (sel->mode == SA_SELECT_MASS && !(sel->mass > 0.0 && sel->mass <= 1.0)) return SA_ERR_INVALID_ARG;
-  if (!q || !k || !row_ptr || !workspace || col_capacity < 0) return SA_ERR_INVALID_ARG;
-  if (stat >= 0 && (!lse || !aligned(lse, 4))) return SA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(row_ptr, 8) || !aligned(workspace, 256) ||
-      (col_idx && !aligned(col_idx, 4)))
-    return SA_ERR_INVALID_ARG;
-  const sa::BuildLayout L = sa::build_layout(dims.rows, p->Nk, p->d);
-  if (workspace_bytes < L.total) return SA_ERR_INVALID_ARG;
-  const int64_t max_nnz = dims.rows * p->Nk;
-  if (sel->mode == SA_SELECT_TOPK) {
-    const int64_t kk = sel->topk < p->Nk ? sel->topk : p->Nk;
-    if (dims.rows * kk > col_capacity) {
-      if (nnz_out_host) *nnz_out_host = dims.rows * kk;
-      return SA_ERR_CAPACITY;
-    }
-  } else if (col_capacity < max_nnz && !nnz_out_host) {
-    return SA_ERR_INVALID_ARG;  // data-dependent nnz needs the synchronous report
-  }
-  if (col_capacity > 0 && !col_idx) return SA_ERR_INVALID_ARG;
-  int sms = 0;
-  if ((st = device_info(&sms)) != SA_OK) return st;
-  const uint64_t qbytes = uint64_t(p->B) * p->H * p->Nq * p->d * 2;
-  const uint64_t kbytes = uint64_t(p->B) * p->H * p->Nk * p->d * 2;
-  if (!in_device_allocation(q, qbytes) || !in_device_allocation(k, kbytes) ||
-      !in_device_allocation(row_ptr, uint64_t(dims.rows + 1) * 8) ||
-      !in_device_allocation(workspace, L.total) ||
-      (stat >= 0 && !in_device_allocation(lse, uint64_t(p->B) * p->H * p->Nq * 4)) ||
-      (col_capacity > 0 && !in_device_allocation(col_idx, uint64_t(col_capacity) * 4)))
-    return SA_ERR_INVALID_ARG;
-
+  if (!workspace || !aligned(workspace, 256)) return SA_ERR_INVALID_ARG;
   sa::BuildArgs a;
-  a.q = static_cast<const uint16_t*>(q);
-  a.k = static_cast<const uint16_t*>(k);
-  a.lse = lse;
-  a.stat = stat;
-  a.row_ptr = row_ptr;
-  a.col_idx = col_idx;
-  a.col_capacity = col_capacity;
+  int sms = 0;
+  sa_status st = sa::prepare_build(p, sel, stat, q, k, lse, row_ptr, col_idx, col_capacity, nnz_out_host,
+                                   workspace_bytes, SA_ERR_INVALID_ARG, &a, &sms);
+  if (st != SA_OK) return st;
+  if (!in_device_allocation(workspace, a.L.total)) return SA_ERR_INVALID_ARG;
   a.ws = static_cast<uint8_t*>(workspace);
-  a.L = L;
-  a.rows = dims.rows;
-  a.G = dims.G;
-  a.BH = p->B * p->H;
-  a.Nq = p->Nq;
-  a.Nk = p->Nk;
-  a.d = p->d;
-  a.M = p->group_size;
-  a.scale = p->scale;
-  a.mode = sel->mode;
-  a.topk = sel->topk;
-  a.threshold = sel->threshold;
-  a.mass = sel->mass;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = map_cuda(sa::launch_build_index(a, sms, s))) != SA_OK) return st;
-  if (nnz_out_host) {
-    int64_t misc[2] = {0, 0};
-    if (cudaMemcpyAsync(misc, a.ws + L.misc, sizeof misc, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess)
-      return SA_ERR_CUDA;
-    *nnz_out_host = misc[0];
-    const int32_t dev_status = static_cast<int32_t>(misc[1] & 0xFFFFFFFF);
-    if (dev_status & SA_DEVERR_TIMEOUT) return SA_ERR_TIMEOUT;
-    if (dev_status & SA_DEVERR_CAPACITY) return SA_ERR_CAPACITY;
-  }
-  return SA_OK;
+  return sa::run_build(a, sms, nnz_out_host, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // Bit-packed (words) or block (blocks, block_k) masks to CSR.
@@ -234,6 +267,7 @@ sa_status index_from_mask(const sa_problem* p, const uint32_t* words, const uint
   a.Nk = p->Nk;
   a.block_k = words ? 32 : block_k;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  sa::NvtxRange range(words ? "sparse_attn_index_from_bitmask" : "sparse_attn_index_from_block_mask");
   if ((st = map_cuda(sa::launch_index_from_mask(a, sms, s))) != SA_OK) return st;
   if (nnz_out_host) {
     int64_t nnz = 0;
@@ -323,6 +357,7 @@ sa_status sparse_attn_forward(const sa_problem* p, const void* q, const void* k,
   int sms = 0;
   sa_status st = forward_args(p, q, k, v, row_ptr, col_idx, nnz, o, lse, dev_status, &a, &sms);
   if (st != SA_OK) return st;
+  sa::NvtxRange range(a.dense ? "sparse_attn_forward (dense)" : "sparse_attn_forward");
   return map_cuda(sa::launch_forward(a, p->d, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -351,6 +386,7 @@ sa_status sparse_attn_forward_delta(const sa_problem* p, const void* q, const vo
   a.lse_ref = lse_ref;
   a.base = base;
   a.sign = sign;
+  sa::NvtxRange range("sparse_attn_forward_delta");
   return map_cuda(sa::launch_forward_delta(a, p->d, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -398,6 +434,7 @@ sa_status sparse_attn_voxel_permute(const sa_voxel_grid* g, int32_t BH, int32_t 
   a.vw = g->vw;
   a.pieces = d / 8;
   a.inverse = inverse;
+  sa::NvtxRange range("sparse_attn_voxel_permute");
   return map_cuda(sa::launch_voxel_permute(a, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -427,6 +464,7 @@ sa_status sparse_attn_kv_window_append(int32_t BH, int32_t d, int32_t chunk_toke
   a.L16 = int64_t(chunk_tokens) * d / 8;
   a.S = slots;
   a.slot = chunks_before < slots ? static_cast<int32_t>(chunks_before) : -1;
+  sa::NvtxRange range("sparse_attn_kv_window_append");
   if ((st = map_cuda(sa::launch_kv_window(a, sms, reinterpret_cast<cudaStream_t>(stream)))) != SA_OK)
     return st;
   if (valid_tokens) *valid_tokens = int64_t(chunks_before + 1 < slots ? chunks_before + 1 : slots) * chunk_tokens;

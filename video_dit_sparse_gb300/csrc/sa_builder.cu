@@ -8,10 +8,19 @@
 //                        accumulated), fp32 in TMEM; written [rows, Nk].
 //                        K and mean-query tiles arrive by 2-D TMA.
 //   3. sa_select_kernel  per row: the selection cut as an exact fp32 value
-//                        (3-level radix descent over order-preserving keys)
-//                        plus how many keys equal to the cut are kept.
+//                        plus how many keys equal to the cut are kept.  A
+//                        strided sample of the row brackets the cut, one pass
+//                        collects the keys inside the bracket (and marks those
+//                        above it), and an exact ranking among them settles it;
+//                        a bracket the sample misses falls back to a ranking
+//                        of the whole row.  TOPK lists are written here.
 //   4. sa_scan_kernel    row_ptr = exclusive prefix sum of the counts.
 //   5. sa_emit_kernel    ascending indices of kept keys into col_idx.
+//   6. TOPK over >= 8192 keys without the score matrix: sample scores of every
+//      8th key (sa_score_kernel), a per-row bracket of the cut
+//      (sa_bracket_kernel), a classifying score pass that marks keys above the
+//      bracket and stores the ones inside it (sa_rowscore_kernel), and the
+//      exact cut and emission (sa_topk_finalize_kernel).
 #include "sa_device.cuh"
 #include "sa_internal.h"
 #include "sa_tma.h"

@@ -103,8 +103,6 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 // Orders generic-proxy shared-memory writes this thread has observed before
 // later async-proxy reads it issues (the tensor core reads operands through
 // the async proxy); used after waiting on a barrier that cp.async completed.
-// Makes this thread's completed generic-proxy shared-memory writes visible to
-// later async-proxy reads (the tensor core reads operands via the async proxy).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -138,18 +136,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// TMA gather of 4 rows (row coordinates r0..r3, columns x..x+63 of a
-// one-row-box map) into 4 consecutive 128-byte rows of shared memory,
-// swizzled by their shared-memory address like any 128B-swizzled box.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, int x, int r0, int r1,
-                                            int r2, int r3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -327,18 +313,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
-  return d;
-}
-
-// Descriptor of an operand without swizzling (8-row x 16-byte core matrices,
-// each 128 contiguous bytes): lbo/sbo are the distances between core matrices
-// along K and along M/N.
-__device__ __forceinline__ uint64_t plain_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
   return d;
 }
 

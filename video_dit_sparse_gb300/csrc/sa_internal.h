@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "sparse_attn.h"
+
 namespace sa {
 
 struct FwdArgs {
@@ -110,6 +112,44 @@ cudaError_t launch_index_from_mask(const FmtArgs& a, int num_sms, cudaStream_t s
 
 // sparse_attn_layer_from_host splits a layer into at most this many chunks.
 constexpr int kMaxPipelineChunks = 64;
+
+// ------------------------------------------------------------ host checks
+// Shared by every entry point (sa_api.cu defines them).
+struct Dims {
+  int64_t G, rows;
+};
+// Shapes, scale, head dim, group size, output dtype and the 32-bit limits
+// (rows of the per-row kernels, TMA row coordinates).
+sa_status check_problem(const sa_problem* p, Dims* dims);
+// The selection rule of a builder call; `stat` < 0 for mean-query scores,
+// else the column statistic (its THRESHOLD range differs).
+sa_status check_select(const sa_problem* p, const sa_select* sel, int32_t stat);
+// Checks that the current device is an sm_103 GPU and gives its SM count;
+// also resolves the driver's address-range query used by in_device_allocation.
+sa_status device_info(int* num_sms);
+// [p, p + bytes) lies inside one device allocation of the current context.
+bool in_device_allocation(const void* p, uint64_t bytes);
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Every argument rule of a builder call except those on the scratch pointer
+// itself: `scratch_bytes` below the problem's workspace size returns
+// `scratch_short`.  Fills `a` (a->ws left null) and the SM count.
+sa_status prepare_build(const sa_problem* p, const sa_select* sel, int32_t stat, const void* q,
+                        const void* k, const float* lse, int64_t* row_ptr, int32_t* col_idx,
+                        int64_t col_capacity, int64_t* nnz_out_host, size_t scratch_bytes,
+                        sa_status scratch_short, BuildArgs* a, int* num_sms);
+// Launches the builder on a.ws; with nnz_out_host, synchronises the stream
+// and reports nnz and the device status.
+sa_status run_build(const BuildArgs& a, int num_sms, int64_t* nnz_out_host, cudaStream_t s);
+
+// A named NVTX range around a host call (shows the entry point's launches
+// in a profiler's timeline; costs nothing measurable without one).
+struct NvtxRange {
+  explicit NvtxRange(const char* name);
+  ~NvtxRange();
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 cudaError_t launch_validate(const int64_t* row_ptr, const int32_t* col_idx, int64_t rows,
                             int64_t nnz, int32_t Nk, int32_t* status, cudaStream_t stream);

@@ -42,7 +42,31 @@ extern "C" sa_status sparse_attn_layer_from_host(
   if (!p || !sel || !q_host || !k_host || !v_host || !o_host || !q_dev || !k_dev || !v_dev || !o_dev)
     return SA_ERR_INVALID_ARG;
   if ((lse_host != nullptr) != (lse_dev != nullptr)) return SA_ERR_INVALID_ARG;
-  if (p->B < 1 || p->H < 1 || p->Nq < 1 || p->Nk < 1 || p->group_size < 1) return SA_ERR_INVALID_ARG;
+  // Every check on the whole layer comes before the first copy is enqueued:
+  // a short or misaligned staging buffer is an INVALID_ARG with nothing on
+  // any stream.
+  sa::Dims dims;
+  sa_status st0 = sa::check_problem(p, &dims);
+  if (st0 != SA_OK) return st0;
+  if ((st0 = sa::check_select(p, sel, -1)) != SA_OK) return st0;
+  if (!sa::aligned(q_dev, 16) || !sa::aligned(k_dev, 16) || !sa::aligned(v_dev, 16) ||
+      !sa::aligned(o_dev, 16) || (lse_dev && !sa::aligned(lse_dev, 4)) || !row_ptr ||
+      !sa::aligned(row_ptr, 8) || !col_idx || !sa::aligned(col_idx, 4) || !workspace ||
+      !sa::aligned(workspace, 256) || col_capacity < 1)
+    return SA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st0 = sa::device_info(&sms)) != SA_OK) return st0;
+  {
+    const uint64_t qb = uint64_t(p->B) * p->H * p->Nq * p->d * 2;
+    const uint64_t kb = uint64_t(p->B) * p->H * p->Nk * p->d * 2;
+    const uint64_t ob = p->out_dtype == SA_OUT_FP32 ? 2 * qb : qb;
+    if (!sa::in_device_allocation(q_dev, qb) || !sa::in_device_allocation(k_dev, kb) ||
+        !sa::in_device_allocation(v_dev, kb) || !sa::in_device_allocation(o_dev, ob) ||
+        (lse_dev && !sa::in_device_allocation(lse_dev, uint64_t(p->B) * p->H * p->Nq * 4)) ||
+        !sa::in_device_allocation(col_idx, uint64_t(col_capacity) * 4) ||
+        !sa::in_device_allocation(workspace, workspace_bytes))
+      return SA_ERR_INVALID_ARG;
+  }
   const int64_t BH = int64_t(p->B) * p->H;
   // Chunk schedule: only the first chunk's copy in and the last chunk's
   // computation and copy out are not hidden, so with more than two heads the
@@ -75,9 +99,11 @@ extern "C" sa_status sparse_attn_layer_from_host(
   cp.H = static_cast<int32_t>(hc);
   const size_t ws_need = sparse_attn_build_index_workspace_size(&cp);
   if (ws_need == 0 || workspace_bytes < ws_need) return SA_ERR_INVALID_ARG;
-  const int64_t G = (int64_t(p->Nq) + p->group_size - 1) / p->group_size;
+  const int64_t G = dims.G;
   const int64_t kmax = sel->mode == SA_SELECT_TOPK ? (sel->topk < p->Nk ? sel->topk : p->Nk) : p->Nk;
   if (col_capacity < hc * G * kmax) return SA_ERR_CAPACITY;  // one chunk's lists, without a sync
+  if (!sa::in_device_allocation(row_ptr, uint64_t(hc * G + 1) * 8)) return SA_ERR_INVALID_ARG;
+  sa::NvtxRange range("sparse_attn_layer_from_host");
   cudaStream_t sc = reinterpret_cast<cudaStream_t>(compute);
   cudaStream_t si = copy_in ? reinterpret_cast<cudaStream_t>(copy_in) : sc;
   cudaStream_t so = copy_out ? reinterpret_cast<cudaStream_t>(copy_out) : sc;
