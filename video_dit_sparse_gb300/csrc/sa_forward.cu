@@ -481,7 +481,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ gather
-    // Thread pt copies 16-byte chunks (pt mod 8) + 8c of tile rows pt/8, +12, ...
+    // Thread pt copies 16-byte chunks (pt mod 8) + 8c of tile rows pt/8, +28, ...
     // Copies never block the gather warps: each stage's "full" barrier is
     // completed by the copies themselves (cp.async.mbarrier.arrive.noinc).
     // The next tile's indices are loaded while this tile's copies are issued
@@ -490,12 +490,14 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     const int pt = threadIdx.x - C::kProdWarp0 * 32;
     const int sub = pt % C::kLanesPerRow;
     const int row0 = pt / C::kLanesPerRow;
-    // shared-memory offset of chunk `sub` of each of this thread's rows (the
-    // chunks sub + 8c lie c column blocks further on)
-    uint32_t dst_off[C::kKVRowsPerThread];
-#pragma unroll
-    for (int i = 0; i < C::kKVRowsPerThread; ++i)
-      dst_off[i] = sw128_offset(row0 + i * C::kRowStep, sub, BN);
+    // Shared-memory offset of chunk `sub` of this thread's i-th row (the
+    // chunks sub + 8c lie c column blocks further on).  The row step is 4
+    // modulo 8, so the swizzle takes two values: two registers, not one per row.
+    static_assert(C::kRowStep % 8 == 4, "row step");
+    const uint32_t off_even = sw128_offset(row0, sub, BN), off_odd = sw128_offset(row0 + 4, sub, BN) - 512;
+    auto dst_off = [&](int i) -> uint32_t {
+      return static_cast<uint32_t>(i * C::kRowStep * 128) + ((i & 1) ? off_odd : off_even);
+    };
     const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
     uint32_t t = 0, un = 0;
     bool bad_index = false;
@@ -536,7 +538,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           const bool ok = in_list && static_cast<uint32_t>(idx[i]) < static_cast<uint32_t>(a.Nk);
           bad_index |= in_list && !ok;
           const uint16_t* src = ok ? src_head + int64_t(idx[i]) * D : any;
-          const uint32_t dst = dst_base + dst_off[i];
+          const uint32_t dst = dst_base + dst_off(i);
 #pragma unroll
           for (int c = 0; c < C::kChunksPerLane; ++c)
             cp_async16(dst + c * BN * 128, src + 64 * c, ok ? 16u : 0u);
