@@ -70,6 +70,25 @@ def test_random_lists_every_length(d, M):
     P.compare_units(q, k, v, M, row_ptr, col, np.arange(rows), o, lse)
 
 
+@pytest.mark.parametrize("d,M,scale", [(128, 128, -1.0 / math.sqrt(128)), (64, 192, -0.3),
+                                       (128, 128, 0.05)])
+def test_scale_of_either_sign(d, M, scale):
+    """Any finite non-zero scale: a negative one negates every score (the
+    softmax then favours the smallest q.k), and the oracle takes the same
+    scale; lists of every length, ragged groups and tiles."""
+    q, k, v = field(1, 2, d, (5, 10, 20), (7, 10, 10), seed=29)
+    G = -(-1000 // M)
+    rows = 2 * G
+    lists = random_lists(rows, 700, seed=31, sizes=[1, 127, 128, 129, 300, 700, 513])
+    row_ptr, col = oracle.to_csr(lists)
+    o, lse, st = run_forward(q, k, v, M, row_ptr, col, scale=scale)
+    assert st == 0
+    P.compare_units(q, k, v, M, row_ptr, col, np.arange(rows), o, lse, scale=scale)
+    # the bf16 launch is the same result rounded
+    o16, _, _ = run_forward(q, k, v, M, row_ptr, col, scale=scale, out_dtype=torch.bfloat16)
+    assert torch.equal(o16, o.to(torch.bfloat16))
+
+
 @pytest.mark.parametrize("d,M", [(128, 128), (64, 192)])
 def test_bf16_output_is_rounded_fp32_output(d, M):
     q, k, v = field(1, 2, d, (5, 10, 20), (7, 10, 10), seed=11)

@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "sa_internal.h"
 #include "sparse_attn.h"
@@ -99,6 +100,48 @@ bool in_device_allocation(const void* p, uint64_t bytes) {
   const CUdeviceptr dp = reinterpret_cast<CUdeviceptr>(p);
   if (fn(&base, &size, dp) != CUDA_SUCCESS) return false;
   return dp >= base && bytes <= size && dp - base <= size - bytes;
+}
+
+// Per device and symbol: the context whose instance of the symbol `addr`
+// points into.  Every CUDA context holds its own copy of a __device__
+// variable, so a call from another context looks the address up again.
+namespace {
+constexpr int kMaxSymbols = 4;
+struct SymbolSlot {
+  CUcontext ctx = nullptr;
+  void* addr = nullptr;
+};
+std::mutex g_sym_mu;
+SymbolSlot g_sym[kMaxDevices][kMaxSymbols];
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn g_ctx_current = nullptr;  // guarded by g_sym_mu
+}  // namespace
+
+sa_status symbol_address(const void* symbol, int id, void** addr) {
+  int dev = 0;
+  if (id < 0 || id >= kMaxSymbols) return SA_ERR_INVALID_ARG;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_sym_mu);
+  if (!g_ctx_current) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return SA_ERR_CUDA;
+    g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return SA_ERR_CUDA;
+  SymbolSlot& s = g_sym[dev][id];
+  if (s.ctx != ctx || !s.addr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || !p) return SA_ERR_CUDA;
+    s.ctx = ctx;
+    s.addr = p;
+  }
+  *addr = s.addr;
+  return SA_OK;
 }
 
 NvtxRange::NvtxRange(const char* name) { nvtxRangePushA(name); }

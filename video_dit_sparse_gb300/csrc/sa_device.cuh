@@ -325,6 +325,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same descriptor with operand B negated (bit 14; bit 13 negates A):
+// D (+)= A * (-B), exact for bf16 operands.
+__host__ __device__ constexpr uint32_t idesc_negate_b(uint32_t idesc) { return idesc | (1u << 14); }
+
 // Byte offset of 16-byte chunk `c` (of a D-element bf16 row) for row `r` of a
 // tile with `rows` rows, in the 128B-swizzled layout: the row is split into
 // 64-element column blocks of rows*128 bytes each; inside a block, row r sits

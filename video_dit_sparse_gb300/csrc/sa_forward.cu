@@ -95,14 +95,47 @@ struct FwdCfg {
   static_assert(kProdThreads % kLanesPerRow == 0 && kChunksPerLane >= 1, "gather mapping");
 };
 
+// The CTA's unit sequence reaches every role through a ring of kRing slots
+// in shared memory: the first gather thread, which starts each unit before
+// any other role, fills the slot of the unit after next once every role has
+// read the slot's previous unit; -1 ends the sequence.  Two slots keep at
+// most one unit drawn ahead of the slowest role, so that units drawn from the
+// shared counter do not pile up in one CTA.
+constexpr int kRing = 2;
+
+// The f-th unit of this CTA: from the launch's counter (dynamic: a CTA that
+// finishes early takes more units, so ragged lists balance), else units
+// b, b + gridDim.x, ...; -1 past the last unit.
+__device__ __forceinline__ int64_t draw_unit(const FwdArgs& a, uint32_t f) {
+  const int64_t u = a.sched ? static_cast<int64_t>(atomicAdd(a.sched, 1u))
+                            : static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(f) * gridDim.x;
+  return u < a.units ? u : -1;
+}
+
 template <int RB, int STAGES>
 struct FwdBars {
   uint64_t kfull[STAGES], vfull[STAGES], kempty[STAGES], vempty[STAGES];
   uint64_t qfull, qempty, drain;
+  uint64_t ring_full[kRing], ring_empty[kRing];
+  int64_t ring_u[kRing];
   uint64_t sfull[2][RB], pfull[2][RB], pvdone[2][RB], ofree[RB];
   uint32_t tmem_base;
   int abort;
 };
+
+// Unit number i of this CTA from the ring (-1: no more units).  Every
+// thread of a reading warp calls it; `release` (one lane per reading warp,
+// after the warp has read the slot) frees the slot for the unit after next.
+template <class Bars>
+__device__ __forceinline__ bool ring_read(Bars* bars, uint32_t i, int64_t* u, bool release,
+                                          volatile int* abort) {
+  const uint32_t s = i % kRing;
+  if (!mbar_wait(&bars->ring_full[s], (i / kRing) & 1, abort)) return false;
+  *u = bars->ring_u[s];
+  __syncwarp(__activemask());
+  if (release) mbar_arrive(&bars->ring_empty[s]);
+  return true;
+}
 
 // Unit u's list bounds.  A malformed row_ptr pair makes the unit empty.
 template <bool DENSE>
@@ -184,6 +217,11 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     mbar_init(&bars->qfull, 1);
     mbar_init(&bars->qempty, 1);
     mbar_init(&bars->drain, 1);
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(&bars->ring_full[r], 1);
+      // one arrival from each reader: the MMA thread, every softmax and gather warp
+      mbar_init(&bars->ring_empty[r], 1 + C::kSoftmaxWarps + C::kProdWarps);
+    }
     for (int b = 0; b < 2; ++b)
       for (int r = 0; r < RB; ++r) {
         mbar_init(&bars->sfull[b][r], 1);
@@ -216,7 +254,10 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     const int row_in_unit = rb * 128 + quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t t = 0, un = 0;
-    for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
+    for (uint32_t i = 0;; ++i) {
+      int64_t u;
+      if (!ring_read(bars, i, &u, lane == 0, abort)) goto done;
+      if (u < 0) break;
       int64_t begin;
       bool bad;
       const int64_t len = unit_list<DENSE>(a, u, &begin, &bad);
@@ -252,20 +293,17 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         const float lr0 = valid ? __ldg(a.lse_ref + bh * a.Nq + grow) : INFINITY;
         m = isfinite(lr0) ? lr0 * 1.4426950408889634f : INFINITY;
       }
-      for (uint32_t j = 0; j < n; ++j) {
+      // One S tile: row max, exponentials, sums, P back into TMEM.
+      auto tile = [&](uint32_t j) -> bool {
         const uint32_t tt = t + j, b = C::sbuf(tt);
         const int nvalid = static_cast<int>(min64(BN, len - int64_t(j) * BN));
-        if (!mbar_wait(&bars->sfull[b][rb], C::sphase(tt), abort)) goto done;
+        if (!mbar_wait(&bars->sfull[b][rb], C::sphase(tt), abort)) return false;
         tc_fence_after();
         const uint32_t sbase = tmem + lane_base + b * C::kSCols + rb * BN;
         float x[BN];
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) tmem_ld32(sbase + c * 32, reinterpret_cast<uint32_t*>(x + c * 32));
         tmem_ld_wait();
-        if (a.neg_scale) {
-#pragma unroll
-          for (int c = 0; c < BN; ++c) x[c] = -x[c];
-        }
         if (nvalid < BN) {  // tail tile: columns past the list do not exist
 #pragma unroll
           for (int c = 0; c < BN; ++c)
@@ -291,7 +329,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         } else if (__any_sync(0xffffffffu, mx > m + C::kRescaleLog2)) {
           // O must hold PV of the previous tile before it is rescaled.
           const uint32_t tp = tt - 1;
-          if (!mbar_wait(&bars->pvdone[C::sbuf(tp)][rb], C::sphase(tp), abort)) goto done;
+          if (!mbar_wait(&bars->pvdone[C::sbuf(tp)][rb], C::sphase(tp), abort)) return false;
           tc_fence_after();
           float alpha = 1.f;
           if (mx > m + C::kRescaleLog2) {
@@ -347,7 +385,10 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->pfull[b][rb]);
-      }
+        return true;
+      };
+      for (uint32_t j = 0; j < n; ++j)
+        if (!tile(j)) goto done;
       {
         const uint32_t tl = t + n - 1;
         if (!mbar_wait(&bars->pvdone[C::sbuf(tl)][rb], C::sphase(tl), abort)) goto done;
@@ -371,7 +412,9 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t kIdescS = idesc_bf16(128, BN, false, false);
+      // a negative scale negates the scores: B (= K) negated inside the MMA
+      const uint32_t kIdescS = a.neg_scale ? idesc_negate_b(idesc_bf16(128, BN, false, false))
+                                           : idesc_bf16(128, BN, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
       // Descriptor halves: the high words are constant, the low word holds the
@@ -420,7 +463,10 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         mma_commit(&bars->vempty[tt % STAGES]);
         return true;
       };
-      for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+      for (uint32_t i = 0; ok; ++i) {
+        int64_t u;
+        if (!ring_read(bars, i, &u, true, abort)) break;
+        if (u < 0) break;
         int64_t begin;
         bool bad;
         const int64_t len = unit_list<DENSE>(a, u, &begin, &bad);
@@ -507,7 +553,27 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     int ia[C::kKVRowsPerThread], ib[C::kKVRowsPerThread], ic[C::kKVRowsPerThread];
 #pragma unroll
     for (int i = 0; i < C::kKVRowsPerThread; ++i) ia[i] = ib[i] = ic[i] = 0;
-    for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
+    // the unit drawn for the ring slot after next (pt 0 only): the counter's
+    // answer is first needed a whole unit after the draw is issued
+    int64_t drawn = -1;
+    if (pt == 0) {
+      bars->ring_u[0] = draw_unit(a, 0);
+      mbar_arrive(&bars->ring_full[0]);
+      if (bars->ring_u[0] >= 0) drawn = draw_unit(a, 1);
+    }
+    for (uint32_t i = 0;; ++i) {
+      int64_t u;
+      if (!ring_read(bars, i, &u, lane == 0, abort)) goto done;
+      if (u < 0) break;
+      if (pt == 0) {
+        // slot i + 1 takes the unit drawn during unit i - 1, once every role
+        // has read its previous unit (i - 1)
+        const uint32_t f = i + 1, s = f % kRing;
+        if (f >= kRing && !mbar_wait(&bars->ring_empty[s], ((f / kRing) - 1) & 1, abort)) goto done;
+        bars->ring_u[s] = drawn;
+        mbar_arrive(&bars->ring_full[s]);
+        if (drawn >= 0) drawn = draw_unit(a, f + 1);
+      }
       int64_t begin;
       bool bad;
       const int64_t len = unit_list<DENSE>(a, u, &begin, &bad);
@@ -628,9 +694,24 @@ static cudaError_t launch(const FwdArgs& a, const CUtensorMap& tmq, int num_sms,
   return cudaGetLastError();
 }
 
+// Unit counters of the dynamic schedule.  Each launch takes the next slot and
+// clears it on its own stream just before the kernel, so launches in flight
+// at the same time count in different slots (as long as fewer than
+// kSchedSlots are in flight at once).
+constexpr int kSchedSlots = 256;
+__device__ uint32_t g_sched[kSchedSlots];
+std::atomic<uint32_t> g_sched_next{0};
+
 template <bool DELTA>
-static cudaError_t launch_any(const FwdArgs& a, int d, int num_sms, cudaStream_t stream) {
+static cudaError_t launch_any(FwdArgs a, int d, int num_sms, cudaStream_t stream) {
   if (a.units <= 0) return cudaSuccess;
+  if (a.units > num_sms) {  // more units than CTAs: draw them dynamically
+    void* base = nullptr;
+    if (symbol_address(g_sched, 1, &base) != SA_OK) return cudaErrorInvalidSymbol;
+    a.sched = static_cast<uint32_t*>(base) + g_sched_next.fetch_add(1) % kSchedSlots;
+    cudaError_t e = cudaMemsetAsync(a.sched, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return e;
+  }
   const int64_t bh = a.units / a.G;
   CUtensorMap tmq;
   if (!make_rows_map(&tmq, a.q, uint64_t(bh) * a.Nq, d, 128)) return cudaErrorInvalidValue;

@@ -23,9 +23,11 @@ struct FwdArgs {
   int64_t G;
   int32_t Nq, Nk, M;
   int32_t out_fp32;
-  int32_t neg_scale;  // scale < 0: scores are negated and scale_log2 = |scale| log2(e)
+  int32_t neg_scale;  // scale < 0: the QK MMA negates K, and scale_log2 = |scale| log2(e)
   float scale_log2;   // |scale| * log2(e)
   int32_t dense = 0;  // no lists: every unit keeps keys 0 .. Nk-1
+  // unit counter of the launch (zero when it starts), or null: static schedule
+  uint32_t* sched = nullptr;
   // sparse delta (launch_forward_delta): o = base + sign * sum_j exp(l_ij - lse_i) v_j
   const float* lse_ref = nullptr;  // [B,H,Nq] natural-log normaliser per query row
   const float* base = nullptr;     // [B,H,Nq,d] fp32 or null (zero)
@@ -141,6 +143,11 @@ sa_status prepare_build(const sa_problem* p, const sa_select* sel, int32_t stat,
 // Launches the builder on a.ws; with nnz_out_host, synchronises the stream
 // and reports nnz and the device status.
 sa_status run_build(const BuildArgs& a, int num_sms, int64_t* nnz_out_host, cudaStream_t s);
+
+// Device address of a __device__ variable (`symbol`, its host-side name) in
+// the current context, looked up once per (device, context) and cached under
+// `id` (0: the builder's fixed scratch, 1: the forward's unit counters).
+sa_status symbol_address(const void* symbol, int id, void** addr);
 
 // A named NVTX range around a host call (shows the entry point's launches
 // in a profiler's timeline; costs nothing measurable without one).

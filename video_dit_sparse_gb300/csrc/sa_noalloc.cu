@@ -24,7 +24,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "sa_internal.h"
 #include "sparse_attn.h"
@@ -32,49 +31,8 @@
 namespace {
 
 constexpr size_t kScratchBytes = SA_NOALLOC_WORKSPACE_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
-
-// Per device: the context whose instance of g_scratch `addr` points into.
-struct ScratchSlot {
-  CUcontext ctx = nullptr;
-  void* addr = nullptr;
-};
-std::mutex g_mu;
-ScratchSlot g_slots[kMaxDevices];
-
-using CtxGetCurrentFn = CUresult (*)(CUcontext*);
-CtxGetCurrentFn g_ctx_current = nullptr;  // guarded by g_mu
-
-// Device address of this context's g_scratch (device_info() has made a
-// context current and checked the device).
-sa_status scratch_for_current_context(void** addr) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return SA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_ctx_current) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-      return SA_ERR_CUDA;
-    g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(fn);
-  }
-  CUcontext ctx = nullptr;
-  if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return SA_ERR_CUDA;
-  ScratchSlot& s = g_slots[dev];
-  if (s.ctx != ctx || !s.addr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return SA_ERR_CUDA;
-    s.ctx = ctx;
-    s.addr = p;
-  }
-  *addr = s.addr;
-  return SA_OK;
-}
 
 }  // namespace
 
@@ -91,7 +49,7 @@ extern "C" sa_status sparse_attn_build_index_noalloc(const sa_problem* p, const 
                                    nnz_out_host, kScratchBytes, SA_ERR_UNSUPPORTED, &a, &sms);
   if (st != SA_OK) return st;
   void* scratch = nullptr;
-  if ((st = scratch_for_current_context(&scratch)) != SA_OK) return st;
+  if ((st = sa::symbol_address(g_scratch, 0, &scratch)) != SA_OK) return st;
   a.ws = static_cast<uint8_t*>(scratch);
   // launch_build_index clears the counters it accumulates into (nnz, status);
   // every other scratch byte it reads is written earlier in the same call.
