@@ -252,6 +252,9 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
     // ------------------------------------------------------------ softmax
     const int rb = warp >> 2, quarter = warp & 3;
     const int row_in_unit = rb * 128 + quarter * 32 + lane;
+    // A warp whose 32 rows lie past every group (the padding rows of a
+    // 192-row group in its second 128-row block) skips the softmax work.
+    const bool idle = rb * 128 + quarter * 32 >= a.M;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t t = 0, un = 0;
     for (uint32_t i = 0;; ++i) {
@@ -298,6 +301,10 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         const uint32_t tt = t + j, b = C::sbuf(tt);
         const int nvalid = static_cast<int>(min64(BN, len - int64_t(j) * BN));
         if (!mbar_wait(&bars->sfull[b][rb], C::sphase(tt), abort)) return false;
+        if (idle) {  // rows past the group: their P and O are never used
+          mbar_arrive(&bars->pfull[b][rb]);
+          return true;
+        }
         tc_fence_after();
         const uint32_t sbase = tmem + lane_base + b * C::kSCols + rb * BN;
         float x[BN];
@@ -395,12 +402,14 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         tc_fence_after();
         const float inv = DELTA ? a.sign : 1.f / lr;
         const uint32_t obase = tmem + lane_base + C::kOCol + rb * D;
+        if (!idle) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(obase + c * 32, r);
-          tmem_ld_wait();
-          if (valid) store_row32(a, orow_off, c * 32, r, inv, DELTA);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(obase + c * 32, r);
+            tmem_ld_wait();
+            if (valid) store_row32(a, orow_off, c * 32, r, inv, DELTA);
+          }
         }
         if (!DELTA && valid && a.lse) a.lse[bh * a.Nq + grow] = m * 0.69314718055994531f + __logf(l);
         tc_fence_before();
