@@ -1712,12 +1712,12 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const 
     for (int r = lane; r < a.nreg; r += 32) {  // (nreg <= 64)
       above += nab[r];
       const int c = ncd[r];
-      over |= c > a.cap;
+      over |= c > a.cap || c < 0;  // (a negative count: a damaged workspace)
       ntot += c;
     }
     // region offsets in the packed candidate list
-    const int ca = lane < a.nreg ? min(ncd[lane], a.cap) : 0;
-    const int cb = lane + 32 < a.nreg ? min(ncd[lane + 32], a.cap) : 0;
+    const int ca = lane < a.nreg ? max(0, min(ncd[lane], a.cap)) : 0;
+    const int cb = lane + 32 < a.nreg ? max(0, min(ncd[lane + 32], a.cap)) : 0;
     const int ia = warp_incl_scan(ca);
     const int ib = warp_incl_scan(cb) + __shfl_sync(0xffffffffu, ia, 31);
     reg_off[lane + 1] = ia;
@@ -1888,7 +1888,10 @@ __global__ void __launch_bounds__(kSelThreads, 4) sa_topk_finalize_kernel(const 
           keep = before < ties;
         }
       }
-      if (keep) atomicOr(&kept[j >> 5], 1u << (j & 31));
+      // (a key outside [0, Nk), which only a damaged workspace could hold,
+      // sets no bit: the count check below then leaves the row to the
+      // select kernel)
+      if (keep && static_cast<uint32_t>(j) < static_cast<uint32_t>(a.Nk)) atomicOr(&kept[j >> 5], 1u << (j & 31));
     }
   }
   __syncthreads();
