@@ -130,6 +130,31 @@ def test_large_logits_rescale_path():
     P.compare_units(q, k, v, 128, row_ptr, col, [0], o, lse)
 
 
+@pytest.mark.parametrize("case", ["growing16", "late_outlier", "falling"])
+def test_running_max_raised_by_a_later_tile(case):
+    """A later tile whose scores sit far above the running max (set by the
+    unit's first tile) makes its P against that max sum past the lazy-rescale
+    bound: the kernel then takes the tile's max, rescales O and the sums and
+    recomputes P.  Falling scores never raise it."""
+    rng = np.random.default_rng(11)
+    Nk, d = 1024, 128
+    base = rng.standard_normal(d).astype(np.float32)
+    q32 = (base[None, None, None, :] + 0.3 * rng.standard_normal((1, 1, 128, d))).astype(np.float32)
+    k32 = rng.standard_normal((1, 1, Nk, d)).astype(np.float32)
+    if case == "growing16":
+        k32 *= np.linspace(0.05, 16.0, Nk, dtype=np.float32)[None, None, :, None]
+    elif case == "late_outlier":
+        k32[0, 0, 1000] = 3.0 * base  # score ~ 3 |base|^2 / sqrt(d) above every other key's
+    else:
+        k32 *= np.linspace(8.0, 0.05, Nk, dtype=np.float32)[None, None, :, None]
+    q, k = I.f32_to_bf16_bits(q32), I.f32_to_bf16_bits(k32)
+    v = I.f32_to_bf16_bits(rng.standard_normal((1, 1, Nk, d)).astype(np.float32))
+    row_ptr, col = oracle.to_csr([np.arange(Nk, dtype=np.int32)])
+    o, lse, st = run_forward(q, k, v, 128, row_ptr, col)
+    assert st == 0
+    P.compare_units(q, k, v, 128, row_ptr, col, [0], o, lse)
+
+
 def test_permuted_and_duplicate_free_lists_match():
     q, k, v = field(1, 1, 128, (2, 8, 16), (4, 8, 16))
     rng = np.random.default_rng(5)

@@ -14,8 +14,10 @@
 //                 and O += P V with P read from TMEM;
 //   softmax warps keep the running max / sum per query row in registers
 //                 (DiT page, "Online Softmax"), write P as bf16 over S in
-//                 TMEM and rescale O only when the row max grows by more
-//                 than 2^32 (exact after the final division by the sum);
+//                 TMEM and rescale O only when the running max must grow by
+//                 2^32 (exact after the final division by the sum): for
+//                 128-row groups a unit finds a row max in its first tile
+//                 and then only in the rare tiles whose P overflow that bound;
 //                 the epilogue writes O / l in bf16 and lse = m + ln l.
 // The softmax is restricted to the kept keys (Chipmunk review, major
 // comment 1, Alg. 3).  Groups longer than 128 rows (C = 192) use two
@@ -63,9 +65,15 @@ struct FwdCfg {
   static constexpr int kChunksPerLane = (D / 8) / kLanesPerRow;
   static constexpr int kRowStep = kProdThreads / kLanesPerRow;
   static constexpr int kKVRowsPerThread = (BN + kRowStep - 1) / kRowStep;
-  // Lazy rescale: O and the row sums are rescaled only when the row max
-  // grows by more than 2^kRescaleLog2.  P stays <= 2^32 and O, l within fp32.
+  // Lazy rescale: O and the row sums are rescaled only when the running max
+  // must grow (a tile's P against it would sum past 2^kRescaleLog2, or, for
+  // 192-row groups, the tile's max exceeds it by kRescaleLog2).  P stays
+  // <= 2^32 and O, l within fp32.
   static constexpr float kRescaleLog2 = 32.f;
+  static constexpr float kRescaleLimit = 4294967296.f;  // 2^kRescaleLog2
+  // 128-row groups skip the row max of tiles that cannot need it (see the
+  // softmax warps); 192-row groups, with half-width tiles, take every max.
+  static constexpr bool kLazyMax = RB == 1;
   static constexpr int kQBlock = 128 * D * 2;    // one 128-row block of Q
   static constexpr int kQBytes = RB * kQBlock;
   static constexpr int kTile = BN * D * 2;       // one K or V tile
@@ -316,10 +324,9 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           for (int c = 0; c < BN; ++c)
             if (c >= nvalid) x[c] = -INFINITY;
         }
-        // Row max of the raw scores (scale > 0 commutes with max): 3-input
-        // maxima in 8 chains.
-        float mx = 0.f;
-        if (!DELTA) {
+        // Row max of the raw scores (scale > 0 commutes with max), scaled:
+        // 3-input maxima in 8 chains.
+        auto row_max = [&]() -> float {
           float t8[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) t8[i] = fmaxf(x[i], x[8 + i]);
@@ -327,21 +334,47 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           for (int c = 16; c < BN; c += 16)
 #pragma unroll
             for (int i = 0; i < 8; ++i) t8[i] = fmax3(t8[i], x[c + i], x[c + 8 + i]);
-          mx = fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
-        }
-        mx *= sl;
-        if (DELTA) {
-        } else if (j == 0) {
-          m = mx;
-        } else if (__any_sync(0xffffffffu, mx > m + C::kRescaleLog2)) {
+          return sl * fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
+        };
+        // P = exp2(s*x - mm): a packed two-lane FFMA per pair, then EX2.  The
+        // fp32 sum of P gives the log-sum-exp; O is normalised by the sum of
+        // the bf16-rounded P that the PV MMA consumes, so that O stays a
+        // convex combination of V rows whatever the rounding.
+        uint32_t p[BN / 2];
+        uint32_t plo[DELTA ? BN / 2 : 1];
+        auto exps = [&](float mm, float* sum, float* sum_r) {
+          const uint64_t sl2 = f2(sl, sl), nm2 = f2(-mm, -mm);
+          // eight partial sums of each kind: short dependency chains
+          uint64_t ps[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          float pr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < BN / 2; ++c) {
+            const uint64_t y = fma2(f2(x[2 * c], x[2 * c + 1]), sl2, nm2);
+            const float p0 = fast_exp2(f2lo(y)), p1 = fast_exp2(f2hi(y));
+            p[c] = pack_bf16(p0, p1);
+            if (!DELTA) {
+              ps[c & 7] = add2(ps[c & 7], f2(p0, p1));
+              pr[c & 7] = add_bf16x2(p[c], pr[c & 7]);
+            } else {
+              plo[c] = pack_bf16(p0 - __uint_as_float(p[c] << 16), p1 - __uint_as_float(p[c] & 0xFFFF0000u));
+            }
+          }
+          const uint64_t s2 = add2(add2(add2(ps[0], ps[1]), add2(ps[2], ps[3])),
+                                   add2(add2(ps[4], ps[5]), add2(ps[6], ps[7])));
+          *sum = f2lo(s2) + f2hi(s2);
+          *sum_r = ((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7]));
+        };
+        // O, l and lr times 2^(m - mn) with m raised to mn where `raise`
+        // (warp-collective: every lane takes part, alpha = 1 where not raised).
+        auto rescale = [&](bool raise, float mn) -> bool {
           // O must hold PV of the previous tile before it is rescaled.
           const uint32_t tp = tt - 1;
           if (!mbar_wait(&bars->pvdone[C::sbuf(tp)][rb], C::sphase(tp), abort)) return false;
           tc_fence_after();
           float alpha = 1.f;
-          if (mx > m + C::kRescaleLog2) {
-            alpha = fast_exp2(m - mx);
-            m = mx;
+          if (raise) {
+            alpha = fast_exp2(m - mn);
+            m = mn;
           }
           l *= alpha;
           lr *= alpha;
@@ -356,32 +389,35 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
             tmem_st32(obase + c * 32, r);
           }
           tmem_st_wait();
-        }
-        // P = exp2(s*x - m): a packed two-lane FFMA per pair, then EX2.  The
-        // fp32 sum of P gives the log-sum-exp; O is normalised by the sum of
-        // the bf16-rounded P that the PV MMA consumes, so that O stays a
-        // convex combination of V rows whatever the rounding.
-        const uint64_t sl2 = f2(sl, sl), nm2 = f2(-m, -m);
-        uint32_t p[BN / 2];
-        uint32_t plo[DELTA ? BN / 2 : 1];
-        uint64_t ps[4] = {0, 0, 0, 0};
-        float pr[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < BN / 2; ++c) {
-          const uint64_t y = fma2(f2(x[2 * c], x[2 * c + 1]), sl2, nm2);
-          const float p0 = fast_exp2(f2lo(y)), p1 = fast_exp2(f2hi(y));
-          p[c] = pack_bf16(p0, p1);
-          if (!DELTA) {
-            ps[c & 3] = add2(ps[c & 3], f2(p0, p1));
-            pr[c & 3] = add_bf16x2(p[c], pr[c & 3]);
-          } else {
-            plo[c] = pack_bf16(p0 - __uint_as_float(p[c] << 16), p1 - __uint_as_float(p[c] & 0xFFFF0000u));
+          return true;
+        };
+        // The running max m moves only when a tile needs it (lazy rescale);
+        // the first tile of a unit sets it to that tile's max.  128-row
+        // groups: a later tile's P are computed against the current m, and
+        // only when their sum exceeds 2^kRescaleLog2 (so some P might: P >= 0)
+        // does the warp take the tile's exact max, raise m to it, rescale and
+        // compute P again, so most tiles need no row max at all.  192-row
+        // groups (64-key tiles): every tile's max, m raised when it grows by
+        // more than kRescaleLog2.  Every P the PV MMA consumes is
+        // <= 2^kRescaleLog2.
+        float ts = 0.f, tr = 0.f;
+        if (!DELTA && (j == 0 || !C::kLazyMax)) {
+          const float mx = row_max();
+          if (j == 0) {
+            m = mx;
+          } else if (__any_sync(0xffffffffu, mx > m + C::kRescaleLog2)) {
+            if (!rescale(mx > m + C::kRescaleLog2, mx)) return false;
           }
         }
+        exps(m, &ts, &tr);
+        if (C::kLazyMax && !DELTA && j > 0 && __any_sync(0xffffffffu, !(ts <= C::kRescaleLimit))) {
+          const float mx = row_max();
+          if (!rescale(!(ts <= C::kRescaleLimit), fmaxf(m, mx))) return false;
+          exps(m, &ts, &tr);
+        }
         if (!DELTA) {
-          const uint64_t s2 = add2(add2(ps[0], ps[1]), add2(ps[2], ps[3]));
-          l += f2lo(s2) + f2hi(s2);
-          lr += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+          l += ts;
+          lr += tr;
         }
 #pragma unroll
         for (int c = 0; c < BN / 64; ++c) tmem_st32(sbase + c * 32, p + c * 32);
