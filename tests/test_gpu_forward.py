@@ -2,7 +2,7 @@
 C ABI), with index lists given by the test so that the forward is checked on
 its own: random lists of every length (empty, single key, partial tiles,
 several tiles, every key), ragged query groups, d in {64, 128} and group
-sizes 64/128/192/256."""
+sizes 64/128/160/192/224/256."""
 import math
 
 import numpy as np
@@ -56,7 +56,7 @@ def test_tiny_preset_full_compare():
 
 
 @pytest.mark.parametrize("d,M", [(128, 128), (64, 128), (128, 192), (64, 192), (128, 64),
-                                 (128, 256)])
+                                 (128, 256), (128, 160), (64, 224)])
 def test_random_lists_every_length(d, M):
     # Nq = 1000 -> a ragged last group; Nk = 700 -> 6 key tiles, ragged tail
     q, k, v = field(1, 2, d, (5, 10, 20), (7, 10, 10), seed=d + M)

@@ -54,8 +54,13 @@ struct FwdCfg {
   static constexpr int kProdWarps = RB == 1 ? 7 : 3;
   static constexpr int kProdThreads = 32 * kProdWarps;
   static constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProdWarps);
+  // setmaxnreg acts per warpgroup: the four softmax warps (one warpgroup) go
+  // up, the other two warpgroups down.  A split inside a warpgroup never
+  // completes.
   static constexpr bool kRegSplit = RB == 1;
   static constexpr int kRegSoftmax = 240, kRegOther = 80;
+  static_assert(!kRegSplit || (kSoftmaxWarps % 4 == 0 && kThreads % 128 == 0),
+                "register split by whole warpgroups");
   static_assert(!kRegSplit || (kRegSoftmax * 4 + kRegOther * (kThreads / 32 - 4)) * 32 <=
                                   (65536 / kThreads / 8 * 8) * kThreads,
                 "register split exceeds the launch's registers");
