@@ -285,8 +285,10 @@ sa_status sparse_attn_forward_delta(const sa_problem* problem, const void* q, co
  * calls above.)  The B*H (batch, head) pairs are split into chunks of
  * consecutive heads: with more than two heads the first and the last chunk
  * hold one head each (their copies are the ones computation cannot hide)
- * and the heads between form chunks of heads_per_chunk (0: the middle split
- * in three); at most 64 chunks.  For each chunk, on copy_in: Q, K, V from
+ * and the heads between form chunks of 1, 2, 4, ... heads up to
+ * heads_per_chunk (0: the middle split in three), then heads_per_chunk, so
+ * that each chunk's copy in is hidden behind the previous chunk's
+ * computation from the start; at most 64 chunks.  For each chunk, on copy_in: Q, K, V from
  * host to the device staging buffers; on compute, once they have landed:
  * sparse_attn_build_index (this select, no synchronisation) and
  * sparse_attn_forward; on copy_out, once that is done: O (and LSE) back to

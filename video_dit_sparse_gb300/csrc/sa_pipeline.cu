@@ -70,20 +70,25 @@ extern "C" sa_status sparse_attn_layer_from_host(
   const int64_t BH = int64_t(p->B) * p->H;
   // Chunk schedule: only the first chunk's copy in and the last chunk's
   // computation and copy out are not hidden, so with more than two heads the
-  // first and the last chunk hold one head each and the heads between them
-  // form chunks of hc heads (default: the middle split in three).
+  // first and the last chunk hold one head each.  The heads between them
+  // form chunks of 1, 2, 4, ... heads up to hc (default: the middle split in
+  // three), then hc: a chunk's copy in then takes about as long as the
+  // computation of the chunk before it (a head's copy is shorter than its
+  // computation), so the compute stream does not wait for a large first
+  // copy.
   const int64_t mid = BH > 2 ? BH - 2 : 0;
   int64_t hc = heads_per_chunk > 0 ? heads_per_chunk : (mid > 0 ? (mid + 2) / 3 : BH);
   if (hc > BH) hc = BH;
   int64_t starts[sa::kMaxPipelineChunks + 1];
   int64_t nchunks = 0;
   {
-    int64_t h = 0;
+    int64_t h = 0, size = mid > 0 ? 1 : hc;
     if (mid > 0) starts[nchunks++] = h++;
     while (h < BH - (mid > 0 ? 1 : 0)) {
       if (nchunks >= sa::kMaxPipelineChunks) return SA_ERR_UNSUPPORTED;
       starts[nchunks++] = h;
-      h += hc;
+      h += size < hc ? size : hc;
+      size *= 2;
       if (mid > 0 && h > BH - 1) h = BH - 1;
     }
     if (mid > 0) {
