@@ -79,6 +79,10 @@ struct FwdCfg {
   // 128-row groups skip the row max of tiles that cannot need it (see the
   // softmax warps); 192-row groups, with half-width tiles, take every max.
   static constexpr bool kLazyMax = RB == 1;
+  // groups of more than 128 rows with 128-key tiles: each softmax thread
+  // takes its row's tile in two 64-key halves (a 128-float row would not fit
+  // the 168 registers of a 12-warp block without a register split)
+  static constexpr bool kHalves = RB == 2 && BN == 128;
   static constexpr int kQBlock = 128 * D * 2;    // one 128-row block of Q
   static constexpr int kQBytes = RB * kQBlock;
   static constexpr int kTile = BN * D * 2;       // one K or V tile
@@ -320,6 +324,128 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         }
         tc_fence_after();
         const uint32_t sbase = tmem + lane_base + b * C::kSCols + rb * BN;
+        // O, l and lr times 2^(m - mn) with m raised to mn where `raise`
+        // (warp-collective: every lane takes part, alpha = 1 where not raised).
+        auto rescale = [&](bool raise, float mn) -> bool {
+          // O must hold PV of the previous tile before it is rescaled.
+          const uint32_t tp = tt - 1;
+          if (!mbar_wait(&bars->pvdone[C::sbuf(tp)][rb], C::sphase(tp), abort)) return false;
+          tc_fence_after();
+          float alpha = 1.f;
+          if (raise) {
+            alpha = fast_exp2(m - mn);
+            m = mn;
+          }
+          l *= alpha;
+          lr *= alpha;
+          const uint32_t obase = tmem + lane_base + C::kOCol + rb * D;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(obase + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(obase + c * 32, r);
+          }
+          tmem_st_wait();
+          return true;
+        };
+        if constexpr (C::kHalves) {
+          static_assert(!DELTA && BN == 128, "half tiles: 128-key tiles without the delta");
+          // The tile in two 64-key halves (keys 0-63 in S columns 0-63, keys
+          // 64-127 in 64-127): a thread holds one half's scores and both
+          // halves' P, which is stored only once the tile's sum check has
+          // passed (the slow path reloads the first half's scores from S).
+          constexpr int H = BN / 2;
+          float x[H];
+          uint32_t pa[H / 2], pb[H / 2];
+          uint64_t ps[4];
+          float pr[4];
+          auto load_half = [&](int h) {
+#pragma unroll
+            for (int c = 0; c < H / 32; ++c)
+              tmem_ld32(sbase + h * H + c * 32, reinterpret_cast<uint32_t*>(x + c * 32));
+            tmem_ld_wait();
+            if (nvalid < (h + 1) * H) {  // tail tile: columns past the list do not exist
+#pragma unroll
+              for (int c = 0; c < H; ++c)
+                if (h * H + c >= nvalid) x[c] = -INFINITY;
+            }
+          };
+          auto half_max = [&]() -> float {  // scaled max of the half in x
+            float t8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t8[i] = fmaxf(x[i], x[8 + i]);
+#pragma unroll
+            for (int c = 16; c < H; c += 16)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) t8[i] = fmax3(t8[i], x[c + i], x[c + 8 + i]);
+            return sl * fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmaxf(t8[6], t8[7]));
+          };
+          auto half_exps = [&](float mm, uint32_t* pp) {  // P of the half in x, into the sums
+            const uint64_t sl2 = f2(sl, sl), nm2 = f2(-mm, -mm);
+#pragma unroll
+            for (int c = 0; c < H / 2; ++c) {
+              const uint64_t y = fma2(f2(x[2 * c], x[2 * c + 1]), sl2, nm2);
+              const float p0 = fast_exp2(f2lo(y)), p1 = fast_exp2(f2hi(y));
+              pp[c] = pack_bf16(p0, p1);
+              ps[c & 3] = add2(ps[c & 3], f2(p0, p1));
+              pr[c & 3] = add_bf16x2(pp[c], pr[c & 3]);
+            }
+          };
+          auto zero_sums = [&]() {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              ps[i] = 0;
+              pr[i] = 0.f;
+            }
+          };
+          float ts, tr;
+          auto tile_sums = [&]() {
+            const uint64_t s2 = add2(add2(ps[0], ps[1]), add2(ps[2], ps[3]));
+            ts = f2lo(s2) + f2hi(s2);
+            tr = (pr[0] + pr[1]) + (pr[2] + pr[3]);
+          };
+          zero_sums();
+          if (j == 0) {  // the unit's first tile sets the running max
+            load_half(0);
+            float mx = half_max();
+            load_half(1);
+            mx = fmaxf(mx, half_max());
+            m = mx;
+            half_exps(m, pb);
+            load_half(0);
+            half_exps(m, pa);
+          } else {
+            load_half(0);
+            half_exps(m, pa);
+            load_half(1);
+            half_exps(m, pb);
+          }
+          tile_sums();
+          if (j > 0 && __any_sync(0xffffffffu, !(ts <= C::kRescaleLimit))) {
+            float mx = half_max();  // the second half, still in x
+            load_half(0);
+            mx = fmaxf(mx, half_max());
+            if (!rescale(!(ts <= C::kRescaleLimit), fmaxf(m, mx))) return false;
+            zero_sums();
+            load_half(0);  // (again: no scores are held across the rescale)
+            half_exps(m, pa);
+            load_half(1);
+            half_exps(m, pb);
+            tile_sums();
+          }
+          l += ts;
+          lr += tr;
+          // P of keys 0-63 to columns 0-31, of keys 64-127 to columns 32-63
+          tmem_st32(sbase, pa);
+          tmem_st32(sbase + 32, pb);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->pfull[b][rb]);
+          return true;
+        } else {
         float x[BN];
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) tmem_ld32(sbase + c * 32, reinterpret_cast<uint32_t*>(x + c * 32));
@@ -369,33 +495,6 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           *sum = f2lo(s2) + f2hi(s2);
           *sum_r = ((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7]));
         };
-        // O, l and lr times 2^(m - mn) with m raised to mn where `raise`
-        // (warp-collective: every lane takes part, alpha = 1 where not raised).
-        auto rescale = [&](bool raise, float mn) -> bool {
-          // O must hold PV of the previous tile before it is rescaled.
-          const uint32_t tp = tt - 1;
-          if (!mbar_wait(&bars->pvdone[C::sbuf(tp)][rb], C::sphase(tp), abort)) return false;
-          tc_fence_after();
-          float alpha = 1.f;
-          if (raise) {
-            alpha = fast_exp2(m - mn);
-            m = mn;
-          }
-          l *= alpha;
-          lr *= alpha;
-          const uint32_t obase = tmem + lane_base + C::kOCol + rb * D;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(obase + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(obase + c * 32, r);
-          }
-          tmem_st_wait();
-          return true;
-        };
         // The running max m moves only when a tile needs it (lazy rescale);
         // the first tile of a unit sets it to that tile's max.  128-row
         // groups: a later tile's P are computed against the current m, and
@@ -434,6 +533,7 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         tc_fence_before();
         mbar_arrive(&bars->pfull[b][rb]);
         return true;
+        }
       };
       for (uint32_t j = 0; j < n; ++j)
         if (!tile(j)) goto done;
@@ -765,12 +865,17 @@ static cudaError_t launch_any(FwdArgs a, int d, int num_sms, cudaStream_t stream
   const int64_t bh = a.units / a.G;
   CUtensorMap tmq;
   if (!make_rows_map(&tmq, a.q, uint64_t(bh) * a.Nq, d, 128)) return cudaErrorInvalidValue;
+  // groups of more than 128 rows: 128-key tiles in halves (Q then stays in
+  // shared memory: two S blocks and two O blocks fill TMEM), except for the
+  // delta, whose P needs both bf16 terms at once (64-key tiles)
   if (d == 128) {
-    return a.M <= 128 ? launch<128, 1, 128, 3, DELTA>(a, tmq, num_sms, stream)
-                      : launch<128, 2, 64, 4, DELTA>(a, tmq, num_sms, stream);
+    if (a.M <= 128) return launch<128, 1, 128, 3, DELTA>(a, tmq, num_sms, stream);
+    if constexpr (DELTA) return launch<128, 2, 64, 4, DELTA>(a, tmq, num_sms, stream);
+    else return launch<128, 2, 128, 2, DELTA>(a, tmq, num_sms, stream);
   }
-  return a.M <= 128 ? launch<64, 1, 128, 4, DELTA>(a, tmq, num_sms, stream)
-                    : launch<64, 2, 64, 4, DELTA>(a, tmq, num_sms, stream);
+  if (a.M <= 128) return launch<64, 1, 128, 4, DELTA>(a, tmq, num_sms, stream);
+  if constexpr (DELTA) return launch<64, 2, 64, 4, DELTA>(a, tmq, num_sms, stream);
+  else return launch<64, 2, 128, 4, DELTA>(a, tmq, num_sms, stream);
 }
 
 cudaError_t launch_forward(const FwdArgs& a, int d, int num_sms, cudaStream_t stream) {
