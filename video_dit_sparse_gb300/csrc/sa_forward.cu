@@ -21,7 +21,9 @@
 //                 the epilogue writes O / l in bf16 and lse = m + ln l.
 // The softmax is restricted to the kept keys (Chipmunk review, major
 // comment 1, Alg. 3).  Groups longer than 128 rows (C = 192) use two
-// 128-row blocks that share every K/V tile.  Without index lists every unit
+// 128-row blocks that share every K/V tile: 128-key tiles, each softmax
+// thread working its row in two 64-key halves, Q read from shared memory
+// (the delta: 64-key tiles, Q in TMEM).  Without index lists every unit
 // keeps all keys in order (dense attention, the dense step of a cached
 // mask).
 //
@@ -42,15 +44,15 @@ namespace sa {
 
 template <int D, int RB, int BN, int STAGES>
 struct FwdCfg {
-  // 4*RB softmax warps, one MMA-issuing warp, three gather warps.  (A block
-  // of at most 8 warps lets ptxas give a thread up to 255 registers: the
-  // 128-float S row of a softmax thread must not spill.)
+  // 4*RB softmax warps (one per 32 rows of each 128-row block), one
+  // MMA-issuing warp, then the gather warps.
   static constexpr int kSoftmaxWarps = 4 * RB;
   static constexpr int kMmaWarp = kSoftmaxWarps;
   static constexpr int kProdWarp0 = kSoftmaxWarps + 1;
   // 128-row groups: seven gather warps (12 warps in all), with the softmax
-  // warpgroup's registers raised and the rest lowered after launch; 192-row
-  // groups: three (their eight softmax warps fill the register file).
+  // warpgroup's registers raised (its threads hold a 128-float S row) and the
+  // rest lowered after launch; longer groups: three, no split (their eight
+  // softmax warps hold half rows, or 64-key tiles for the delta).
   static constexpr int kProdWarps = RB == 1 ? 7 : 3;
   static constexpr int kProdThreads = 32 * kProdWarps;
   static constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProdWarps);
@@ -76,8 +78,9 @@ struct FwdCfg {
   // <= 2^32 and O, l within fp32.
   static constexpr float kRescaleLog2 = 32.f;
   static constexpr float kRescaleLimit = 4294967296.f;  // 2^kRescaleLog2
-  // 128-row groups skip the row max of tiles that cannot need it (see the
-  // softmax warps); 192-row groups, with half-width tiles, take every max.
+  // Tiles that cannot need a row max skip it (see the softmax warps): the
+  // 128-row path here, the half-tile path (kHalves) by the same sum check;
+  // the 64-key tiles of longer groups (the delta) have a fixed normaliser.
   static constexpr bool kLazyMax = RB == 1;
   // groups of more than 128 rows with 128-key tiles: each softmax thread
   // takes its row's tile in two 64-key halves (a 128-float row would not fit
@@ -90,8 +93,9 @@ struct FwdCfg {
   // 128-row groups double-buffer S; with two row blocks each block has one S
   // buffer (the MMA warp issues PV(j-1) of a block before QK(j) of the same
   // block, so the tensor core, which runs one thread's MMAs in order, reads P
-  // before S is overwritten) and Q fits in TMEM: the QK MMAs then read only K
-  // from shared memory.
+  // before S is overwritten).  Where Q fits in TMEM beside S and O (below),
+  // the QK MMAs read only K from shared memory; otherwise (two row blocks of
+  // 128-key tiles) they read Q from its shared-memory tile.
   static constexpr int kSBufs = RB == 2 ? 1 : 2;
   static constexpr int kOCol = kSBufs * kSCols;
   static __device__ __forceinline__ uint32_t sbuf(uint32_t tt) { return kSBufs == 2 ? (tt & 1u) : 0u; }
