@@ -22,8 +22,8 @@
 // The softmax is restricted to the kept keys (Chipmunk review, major
 // comment 1, Alg. 3).  Groups longer than 128 rows (C = 192) use two
 // 128-row blocks that share every K/V tile: 128-key tiles, each softmax
-// thread working its row in two 64-key halves, Q read from shared memory
-// (the delta: 64-key tiles, Q in TMEM).  Without index lists every unit
+// thread working its row in two 64-key halves, Q read from shared memory.
+// Without index lists every unit
 // keeps all keys in order (dense attention, the dense step of a cached
 // mask).
 //
@@ -52,7 +52,7 @@ struct FwdCfg {
   // 128-row groups: seven gather warps (12 warps in all), with the softmax
   // warpgroup's registers raised (its threads hold a 128-float S row) and the
   // rest lowered after launch; longer groups: three, no split (their eight
-  // softmax warps hold half rows, or 64-key tiles for the delta).
+  // softmax warps hold half rows).
   static constexpr int kProdWarps = RB == 1 ? 7 : 3;
   static constexpr int kProdThreads = 32 * kProdWarps;
   static constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProdWarps);
@@ -79,8 +79,8 @@ struct FwdCfg {
   static constexpr float kRescaleLog2 = 32.f;
   static constexpr float kRescaleLimit = 4294967296.f;  // 2^kRescaleLog2
   // Tiles that cannot need a row max skip it (see the softmax warps): the
-  // 128-row path here, the half-tile path (kHalves) by the same sum check;
-  // the 64-key tiles of longer groups (the delta) have a fixed normaliser.
+  // 128-row path here, the half-tile path (kHalves) by the same sum check
+  // (the delta has a fixed normaliser: no max at all).
   static constexpr bool kLazyMax = RB == 1;
   // groups of more than 128 rows with 128-key tiles: each softmax thread
   // takes its row's tile in two 64-key halves (a 128-float row would not fit
@@ -355,8 +355,42 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
           tmem_st_wait();
           return true;
         };
-        if constexpr (C::kHalves) {
-          static_assert(!DELTA && BN == 128, "half tiles: 128-key tiles without the delta");
+        if constexpr (C::kHalves && DELTA) {
+          // The delta's tile in two 64-key halves, each finished before the
+          // next is loaded (a fixed normaliser needs no check): its P as bf16
+          // hi and remainder goes to the half's own S columns (hi to the first
+          // 32, remainder to the last 32), which the PV MMAs read that way.
+          constexpr int H = BN / 2;
+          const uint64_t sl2 = f2(sl, sl), nm2 = f2(-m, -m);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float x[H];
+#pragma unroll
+            for (int c = 0; c < H / 32; ++c)
+              tmem_ld32(sbase + h * H + c * 32, reinterpret_cast<uint32_t*>(x + c * 32));
+            tmem_ld_wait();
+            if (nvalid < (h + 1) * H) {  // tail tile: columns past the list do not exist
+#pragma unroll
+              for (int c = 0; c < H; ++c)
+                if (h * H + c >= nvalid) x[c] = -INFINITY;
+            }
+            uint32_t phi[H / 2], plo[H / 2];
+#pragma unroll
+            for (int c = 0; c < H / 2; ++c) {
+              const uint64_t y = fma2(f2(x[2 * c], x[2 * c + 1]), sl2, nm2);
+              const float p0 = fast_exp2(f2lo(y)), p1 = fast_exp2(f2hi(y));
+              phi[c] = pack_bf16(p0, p1);
+              plo[c] = pack_bf16(p0 - __uint_as_float(phi[c] << 16), p1 - __uint_as_float(phi[c] & 0xFFFF0000u));
+            }
+            tmem_st32(sbase + h * H, phi);
+            tmem_st32(sbase + h * H + H / 2, plo);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->pfull[b][rb]);
+          return true;
+        } else if constexpr (C::kHalves) {
+          static_assert(BN == 128, "half tiles: 128-key tiles");
           // The tile in two 64-key halves (keys 0-63 in S columns 0-63, keys
           // 64-127 in 64-127): a thread holds one half's scores and both
           // halves' P, which is stored only once the tile's sum check has
@@ -596,14 +630,21 @@ __global__ void __launch_bounds__(FwdCfg<D, RB, BN, STAGES>::kThreads, 1)
         const uint32_t a_tmem = tmem + b * C::kSCols + rb * BN;
         const uint32_t d_tmem = tmem + C::kOCol + rb * D;
         const uint32_t vs_lo = v_lo + ((s * C::kTile) >> 4);
+        // P of keys 16kk..16kk+15: columns 8kk.. of the S buffer; the delta's
+        // remainder in the second half of the buffer, or, for half tiles, each
+        // 64-key half's P hi then remainder in that half's columns
+        auto p_col = [&](int kk, bool rem) -> uint32_t {
+          if (C::kHalves && DELTA) return (kk >> 2) * (BN / 2) + (rem ? BN / 4 : 0) + (kk & 3) * 8;
+          return (rem ? BN / 2 : 0) + kk * 8;
+        };
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts_w(d_tmem, a_tmem + kk * 8, vs_lo + ((kk * 2048) >> 4), v_hi, kIdescPV,
+          mma_ts_w(d_tmem, a_tmem + p_col(kk, false), vs_lo + ((kk * 2048) >> 4), v_hi, kIdescPV,
                    (!first || kk > 0) ? 1u : 0u);
-        if (DELTA) {  // the remainder of P, from the second half of the S buffer
+        if (DELTA) {  // the remainder of P
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts_w(d_tmem, a_tmem + BN / 2 + kk * 8, vs_lo + ((kk * 2048) >> 4), v_hi, kIdescPV, 1u);
+            mma_ts_w(d_tmem, a_tmem + p_col(kk, true), vs_lo + ((kk * 2048) >> 4), v_hi, kIdescPV, 1u);
         }
         mma_commit(&bars->pvdone[b][rb]);
         return true;
@@ -870,16 +911,13 @@ static cudaError_t launch_any(FwdArgs a, int d, int num_sms, cudaStream_t stream
   CUtensorMap tmq;
   if (!make_rows_map(&tmq, a.q, uint64_t(bh) * a.Nq, d, 128)) return cudaErrorInvalidValue;
   // groups of more than 128 rows: 128-key tiles in halves (Q then stays in
-  // shared memory: two S blocks and two O blocks fill TMEM), except for the
-  // delta, whose P needs both bf16 terms at once (64-key tiles)
+  // shared memory: two S blocks and two O blocks fill TMEM)
   if (d == 128) {
-    if (a.M <= 128) return launch<128, 1, 128, 3, DELTA>(a, tmq, num_sms, stream);
-    if constexpr (DELTA) return launch<128, 2, 64, 4, DELTA>(a, tmq, num_sms, stream);
-    else return launch<128, 2, 128, 2, DELTA>(a, tmq, num_sms, stream);
+    return a.M <= 128 ? launch<128, 1, 128, 3, DELTA>(a, tmq, num_sms, stream)
+                      : launch<128, 2, 128, 2, DELTA>(a, tmq, num_sms, stream);
   }
-  if (a.M <= 128) return launch<64, 1, 128, 4, DELTA>(a, tmq, num_sms, stream);
-  if constexpr (DELTA) return launch<64, 2, 64, 4, DELTA>(a, tmq, num_sms, stream);
-  else return launch<64, 2, 128, 4, DELTA>(a, tmq, num_sms, stream);
+  return a.M <= 128 ? launch<64, 1, 128, 4, DELTA>(a, tmq, num_sms, stream)
+                    : launch<64, 2, 128, 4, DELTA>(a, tmq, num_sms, stream);
 }
 
 cudaError_t launch_forward(const FwdArgs& a, int d, int num_sms, cudaStream_t stream) {
